@@ -1,0 +1,180 @@
+/*
+ * rwkv7.h -- C ABI of the GB300 (sm_103a) RWKV-7 batched decode library.
+ *
+ * The library runs the batched single-token decode step of an RWKV-7 language
+ * model over a pool of per-sequence state slots, as the continuous-batching
+ * worker of the RWKV-Runner Albatross article does ("连续批处理Worker 主循环":
+ * forward_seq_batch over the organised slot batch, then penalties and
+ * sample_next_tokens_batch), with prefill kept apart from decode as in the
+ * RWKV-Server article ("RWKV 批量推理中 Prefill 的正确打开方式", §五: prefill
+ * prompt[:-1], then decode from prompt[-1]).
+ *
+ * Conventions for every entry point:
+ *  - Return value: RWKV7_OK (0) or a negative RWKV7_E* code; rwkv7_last_error()
+ *    then returns a text description (valid until the next call on the ctx).
+ *  - Ownership: the library owns the weights, the slot pool (recurrent states,
+ *    occurrence counts, sampling parameters) and its scratch memory, all in
+ *    device memory it allocates in rwkv7_create / rwkv7_set_weight.  Pointers
+ *    named d_* are caller-owned DEVICE pointers; h_* / host_* are caller-owned
+ *    HOST pointers.  Nothing is retained after a call returns except inside the
+ *    ctx.
+ *  - Execution: calls taking device pointers are asynchronous and ordered on the
+ *    ctx's CUDA stream (the one given to rwkv7_create, or the legacy default
+ *    stream if NULL).  Errors found on the device (an out-of-range or repeated
+ *    slot, an out-of-range token) are latched in a device word and reported by
+ *    the next rwkv7_synchronize() as RWKV7_EINVAL; the kernels never access
+ *    memory out of bounds because of them.  Calls taking host pointers
+ *    synchronize the stream before they return.
+ *  - Not thread-safe: one ctx is used by one host thread at a time.
+ */
+#ifndef RWKV7_H
+#define RWKV7_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RWKV7_API __attribute__((visibility("default")))
+#else
+#define RWKV7_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RWKV7_OK 0
+#define RWKV7_EINVAL (-1)   /* bad argument: null pointer, size, slot or token out of range */
+#define RWKV7_ESHAPE (-2)   /* weight name unknown or its size does not match the config */
+#define RWKV7_ENOMEM (-3)   /* device or host allocation failed */
+#define RWKV7_ECUDA (-4)    /* a CUDA runtime/driver call failed */
+#define RWKV7_ETIMEOUT (-5) /* a bounded wait inside a kernel gave up */
+#define RWKV7_ESTATE (-6)   /* call out of order (e.g. decode before every weight is set) */
+
+#define RWKV7_MAX_STEP_BATCH 256 /* slots per fused step; larger B is split into sub-steps */
+
+typedef struct rwkv7_ctx rwkv7_ctx;
+
+/* Model shape and pool size.  head_size must be 64; d_model a multiple of 64;
+ * d_ffn a multiple of 64; lora_* multiples of 8; n_slots >= 1. */
+typedef struct {
+    int32_t n_layer, d_model, head_size, d_ffn, vocab;
+    int32_t lora_w, lora_a, lora_v, lora_g;
+    int32_t n_slots;
+} rwkv7_config;
+
+/* Per-slot sampling parameters (defaults of the Albatross adapter: temperature 1,
+ * top_p 0.3, top_k 0 (off), frequency 1, penalty_decay 0.996, presence 0).
+ * greedy != 0 (or temperature <= 0) takes the argmax of the raw logits (lowest
+ * index on ties) and leaves the occurrence counts untouched. */
+typedef struct {
+    float temperature, top_p;
+    int32_t top_k;
+    float presence, frequency, penalty_decay;
+    uint64_t seed;
+    int32_t greedy;
+} rwkv7_sampling;
+
+/* Create a context on the current CUDA device; allocates the slot pool and
+ * scratch.  cuda_stream: a cudaStream_t (may be NULL). */
+RWKV7_API int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out);
+
+/* Free everything the ctx owns (synchronizes its stream first).  NULL is a no-op. */
+RWKV7_API void rwkv7_destroy(rwkv7_ctx *ctx);
+
+RWKV7_API const char *rwkv7_last_error(const rwkv7_ctx *ctx);
+
+/* Copy one named fp16 tensor from host memory into the device weights.  Names
+ * and [out, in] shapes follow the weight-file convention (e.g. "emb" [V, d],
+ * "blocks.3.att.key" [d, d], "blocks.3.ffn.value" [d, d_ffn]).  bytes must be
+ * the tensor's exact size.  Synchronous. */
+RWKV7_API int rwkv7_set_weight(rwkv7_ctx *ctx, const char *name, const void *host_f16, size_t bytes);
+
+/* Read every tensor from an RWKV7W01 weight file (text header, 256-byte aligned
+ * fp16 data) and set it.  Synchronous. */
+RWKV7_API int rwkv7_load_weights(rwkv7_ctx *ctx, const char *path);
+
+/* Slot pool (the Albatross worker keeps one state slot per active sequence and
+ * swaps slots when it reorganises the batch; here slots are addressed by index,
+ * so reorganising needs no copies).  Stream-ordered. */
+RWKV7_API int rwkv7_slot_reset(rwkv7_ctx *ctx, int32_t slot);            /* zero state, occurrence counts, draw counter */
+RWKV7_API int rwkv7_slot_swap(rwkv7_ctx *ctx, int32_t a, int32_t b);     /* exchange everything two slots hold */
+RWKV7_API int rwkv7_slot_copy(rwkv7_ctx *ctx, int32_t src, int32_t dst); /* dst := src (prefix-state reuse) */
+RWKV7_API int rwkv7_slot_set_sampling(rwkv7_ctx *ctx, int32_t slot, const rwkv7_sampling *params);
+
+/* Checkpoint of one slot's recurrent state: fp32 wkv [L][H][64][64], then fp32
+ * token-shift states of the time mix [L][d] and of the channel mix [L][d]. */
+RWKV7_API size_t rwkv7_slot_state_bytes(const rwkv7_ctx *ctx);
+RWKV7_API int rwkv7_slot_get_state(rwkv7_ctx *ctx, int32_t slot, void *host_buf, size_t bytes);
+RWKV7_API int rwkv7_slot_set_state(rwkv7_ctx *ctx, int32_t slot, const void *host_buf, size_t bytes);
+
+/* Consume T tokens (device int32 [T]) into one slot.  If d_logits_out is not
+ * NULL it receives the fp32 logits [V] after the last token. */
+RWKV7_API int rwkv7_prefill_seq(rwkv7_ctx *ctx, int32_t slot, const int32_t *d_tokens, int32_t T,
+                      float *d_logits_out);
+
+/* One decode step of B slots: slot d_slots[b] consumes token d_tokens[b]
+ * (device int32 [B] each; slots distinct, 1 <= B <= n_slots).  Writes fp32
+ * logits [B][V] to d_logits_out if not NULL, and if d_next_out is not NULL
+ * samples the next token of every slot with its sampling parameters (updating
+ * its occurrence counts and draw counter) into d_next_out [B]. */
+RWKV7_API int rwkv7_decode_step(rwkv7_ctx *ctx, const int32_t *d_slots, const int32_t *d_tokens,
+                      int32_t B, float *d_logits_out, int32_t *d_next_out);
+
+/* Same step with host buffers (h_logits_out / h_next_out may be NULL): copies
+ * the inputs in, runs the step and copies the results out; synchronous.  Slots
+ * and tokens are checked on the host before anything is launched. */
+RWKV7_API int rwkv7_decode_step_host(rwkv7_ctx *ctx, const int32_t *h_slots, const int32_t *h_tokens,
+                           int32_t B, float *h_logits_out, int32_t *h_next_out);
+
+/* Sample one token per slot from caller logits (device fp32 [B][V]) with the
+ * slots' sampling parameters; updates occurrence counts and draw counters. */
+RWKV7_API int rwkv7_sample_batch(rwkv7_ctx *ctx, const int32_t *d_slots, const float *d_logits,
+                       int32_t B, int32_t *d_next_out);
+
+/* Wait for the ctx's stream and report device-side errors latched since the
+ * last call (RWKV7_EINVAL for bad slots/tokens, RWKV7_ETIMEOUT for a bounded
+ * wait that gave up).  Clears the latched error. */
+RWKV7_API int rwkv7_synchronize(rwkv7_ctx *ctx);
+
+/* Select the decode implementation: 0 = tensor-core kernels with CUDA-graph
+ * replay (default), 1 = the same kernels launched directly, 2 = CUDA-core
+ * (SIMT) projection kernels launched directly (a slow cross-check). */
+RWKV7_API int rwkv7_set_mode(rwkv7_ctx *ctx, int32_t mode);
+
+/* The ctx's own device I/O buffers for a fused step (capacity min(n_slots, 256)
+ * rows): passing these pointers to rwkv7_decode_step skips its staging copies. */
+RWKV7_API int rwkv7_get_io_buffers(rwkv7_ctx *ctx, int32_t **d_slots, int32_t **d_tokens, float **d_logits,
+                         int32_t **d_next);
+
+/* Kernel classes of rwkv7_profile_step, in output order. */
+#define RWKV7_PROF_EMBED 0       /* embedding + LayerNorm 0 (+ slot/token checks) */
+#define RWKV7_PROF_LN_MIX 1      /* LayerNorm + token-shift mixes (time and channel mix) */
+#define RWKV7_PROF_GEMM_PROJ 2   /* r, k, v and LoRA-down projections */
+#define RWKV7_PROF_GEMM_LORA 3   /* LoRA-up projections with decay / gate epilogues */
+#define RWKV7_PROF_WKV 4         /* state update + GroupNorm + bonus + output gate */
+#define RWKV7_PROF_GEMM_OUT 5    /* output projection + residual */
+#define RWKV7_PROF_GEMM_KEY 6    /* channel-mix key + ReLU^2 */
+#define RWKV7_PROF_GEMM_VALUE 7  /* channel-mix value (nonzero blocks) + residual */
+#define RWKV7_PROF_LN_OUT 8      /* final LayerNorm */
+#define RWKV7_PROF_GEMM_HEAD 9   /* head projection to fp32 logits */
+#define RWKV7_PROF_SAMPLER 10    /* penalties + sampling */
+#define RWKV7_PROF_CLASSES 11
+
+/* Run one step of B <= min(n_slots, 256) slots with every kernel launched
+ * directly (no graph, no dependent-launch overlap) and bracketed by CUDA events
+ * on the ctx stream; ms_out[n_classes] receives each class's summed device
+ * time and launches_out[n_classes] its launch count.  Synchronous.  The step
+ * updates the slots' states like rwkv7_decode_step (logits stay internal). */
+RWKV7_API int rwkv7_profile_step(rwkv7_ctx *ctx, const int32_t *d_slots, const int32_t *d_tokens,
+                                 int32_t B, int32_t with_sampling, float *ms_out,
+                                 int32_t *launches_out, int32_t n_classes);
+
+/* Number of kernels one decode step of B slots launches (with / without
+ * sampling), for launch accounting. */
+RWKV7_API int32_t rwkv7_step_kernel_count(const rwkv7_ctx *ctx, int32_t B, int32_t with_sampling);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RWKV7_H */

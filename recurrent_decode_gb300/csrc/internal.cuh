@@ -1,0 +1,320 @@
+// internal.cuh -- shared definitions of the sm_103a kernels and the host runtime.
+// Not part of the public ABI (include/rwkv7.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rk {
+
+// ----------------------------------------------------------------------------
+// Device error word bits (latched by kernels, read by rwkv7_synchronize).
+// ----------------------------------------------------------------------------
+enum : uint32_t {
+    ERR_SLOT = 1u,     // slot index out of range
+    ERR_TOKEN = 2u,    // token id out of range
+    ERR_DUP = 4u,      // a slot appears twice in one step
+    ERR_TIMEOUT = 8u,  // a bounded wait gave up
+    ERR_CONFIG = 16u,  // a kernel met a launch configuration it cannot run
+};
+
+constexpr int HS = 64;             // head size
+constexpr int MAX_B = 256;         // slots per fused step
+constexpr int GEMM_TILE_M = 128;   // weight rows per tile (MMA M)
+constexpr int GEMM_TILE_K = 64;    // reduction elements per stage (128 bytes of fp16)
+constexpr int GEMM_MAX_SEG = 8;
+constexpr int GEMM_MAX_MAPS = 16;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bounded waits give up after ~2 s
+
+// Epilogue kinds of the projection GEMM.  acc is the fp32 dot product of one
+// weight row n with one activation row b.
+enum Epi : int {
+    EPI_F32 = 0,         // out f32 = acc
+    EPI_F16 = 1,         // out f16 = acc
+    EPI_F16_TANH = 2,    // out f16 = tanh(acc)
+    EPI_F16_SIGMOID = 3, // out f16 = sigmoid(acc)
+    EPI_DECAY = 4,       // out f32 = exp(-exp(-1/2) * sigmoid(bias[n] + acc))
+    EPI_SIGMOID_BIAS = 5,// out f32 = sigmoid(bias[n] + acc)
+    EPI_RESID = 6,       // out f32 += acc (residual stream)
+    EPI_RELU2 = 7,       // out f16 = relu(acc)^2, plus a nonzero flag per 64 rows
+};
+
+struct GemmSeg {
+    int wmap, xmap;       // tensor-map indices (tensor-core path)
+    int layer;            // layer coordinate of the weight map
+    int rows, K, kb;      // output rows, reduction length, k-blocks of 64
+    int tile0, unit0;     // first global tile / unit of this segment
+    int epi;
+    void *out;
+    int ldo;              // out element index = b * ldo + n
+    const __half *bias;   // [rows] (EPI_DECAY / EPI_SIGMOID_BIAS)
+    const __half *w;      // row-major weights [rows][K] of this layer (SIMT path)
+    const __half *x;      // activations [B][ldx] (SIMT path)
+    int ldx;
+};
+
+struct GemmParams {
+    CUtensorMap maps[GEMM_MAX_MAPS]; // weight and activation maps used by the segments
+    GemmSeg seg[GEMM_MAX_SEG];
+    int nseg, nmaps, ntiles, nunits;
+    int B, npad;                     // slots in the step, MMA N (B rounded up to 16)
+    int stages;                      // smem pipeline depth
+    int prefetch;                    // 1: weights may be fetched before the dependency wait
+    uint32_t *nz_out;                // EPI_RELU2: flag per 64 output rows
+    const uint32_t *nz_skip;         // nonzero flags per k-block of the activations (or null)
+    float *ws;                       // split-K partials [grid][2][npad][128]
+    uint32_t *counters;              // per-tile arrival tickets (left at zero)
+    uint32_t *err;
+};
+
+// Launch helpers (implemented in the .cu files).
+struct LaunchCfg {
+    cudaStream_t stream;
+    bool pdl;   // programmatic dependent launch
+};
+
+void launch_gemm_tc(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e);
+void launch_gemm_simt(const GemmParams &p, const LaunchCfg &lc, cudaError_t *e);
+size_t gemm_tc_smem_bytes(int npad, int stages);
+int gemm_tc_max_smem();
+
+struct ElemParams {
+    int B, d, H, F, V, n_slots, layer, L;
+    const int32_t *slots, *tokens;
+    float *x;                 // residual [B][d]
+    const __half *emb;        // [V][d]
+    const __half *ln_w, *ln_b;
+    const __half *mu[6];      // token-shift mixes
+    __half *xo[6];            // mixed outputs [B][d]
+    float *shift;             // shift state base of this layer [n_slots][d]
+    uint32_t *err;
+};
+
+void launch_embed(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
+void launch_ln_mix(const ElemParams &p, int nmix, const LaunchCfg &lc, cudaError_t *e);
+void launch_ln_out(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
+
+struct WkvParams {
+    int B, d, H, n_slots, layer;
+    const int32_t *slots;
+    const float *r, *k, *v, *dec, *a, *vg, *g;  // [B][d]
+    float *v_first;                              // [B][d]
+    const __half *k_k, *k_a, *r_k, *lnx_w, *lnx_b;
+    float *wkv;                                  // this layer's states [n_slots][H][64][64]
+    __half *z;                                   // [B][d]
+    uint32_t *err;
+};
+void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e);
+
+struct SampleParamsDev {  // device copy of one slot's sampling parameters
+    float temperature, top_p;
+    int32_t top_k;
+    float presence, frequency, penalty_decay;
+    unsigned long long seed;
+    int32_t greedy, pad;
+};
+
+struct SamplerParams {
+    int B, V, n_slots;
+    const int32_t *slots;
+    const float *logits;   // [B][V]
+    float *occ;            // [n_slots][V]
+    const SampleParamsDev *params;  // [n_slots]
+    unsigned long long *ndraw;      // [n_slots]
+    float *lpen;           // scratch [B][V]
+    int32_t *next;         // [B]
+    uint32_t *err;
+};
+void launch_sampler(const SamplerParams &p, const LaunchCfg &lc, cudaError_t *e);
+
+struct SlotOpParams {
+    int op;  // 0 reset, 1 copy src->dst, 2 swap
+    int a, b;
+    int L, n_slots;
+    size_t wkv_per_slot;   // floats per slot per layer
+    size_t d;              // shift floats per slot per layer
+    int V;
+    float *wkv, *shift_att, *shift_ffn, *occ;
+    unsigned long long *ndraw;
+    SampleParamsDev *params;
+};
+void launch_slot_op(const SlotOpParams &p, cudaStream_t s, cudaError_t *e);
+
+}  // namespace rk
+
+// ----------------------------------------------------------------------------
+// Device-side PTX helpers.
+// ----------------------------------------------------------------------------
+#ifdef __CUDACC__
+namespace rk {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Programmatic dependent launch: wait for the preceding grid's completion (and
+// memory), and allow the next grid to be scheduled.  No-ops without PDL.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with `parity`.  Gives up (returns false) after
+// WAIT_LIMIT_NS or as soon as *abort is non-zero.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (gtimer() - t0 > WAIT_LIMIT_NS) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+}
+
+// TMA tiled loads into shared memory, completing transaction bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1,
+                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(m), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1,
+                                            int c2, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+// ---- tcgen05 (5th-generation tensor cores, accumulators in tensor memory) ----
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on `bar` once every previously issued tcgen05.mma of this thread completes.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+// 32 lanes x 16 columns of 32-bit accumulator words: lane i of the warp gets
+// TMEM lane (base lane + i), columns [col, col + 16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored as rows of
+// 128 bytes (64 fp16) with the 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= (uint64_t)1 << 16;                       // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;             // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;                       // descriptor version (sm_100 family)
+    d |= (uint64_t)2 << 61;                       // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16 with fp16 A/B, fp32 D, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace rk
+#endif

@@ -1,0 +1,970 @@
+// rwkv7_api.cu -- host runtime behind include/rwkv7.h: device weights, the slot
+// pool, activation buffers, TMA descriptors, the per-step launch sequence and
+// its CUDA-graph cache.
+//
+// One decode step of B slots (RWKV-Runner Albatross article, "连续批处理Worker
+// 主循环": forward_seq_batch then sample_next_tokens_batch) launches
+//   embed+LN0 | per layer: LN1+mix6, G1 (r,k,v + LoRA down), G2 (LoRA up +
+//   gates), WKV7+GroupNorm+gate, G3 (output + residual), LN2+mix, G4 (key,
+//   ReLU^2), G5 (value + residual, skipping all-zero hidden blocks) |
+//   LN_out, head, sampler
+// with programmatic dependent launch between kernels so each kernel's weight
+// prefetch overlaps its predecessor's tail, replayed from a CUDA graph per
+// (B, head, sampling) combination.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/rwkv7.h"
+#include "internal.cuh"
+
+using namespace rk;
+
+namespace {
+
+// ---------------------------------------------------------------- weights
+enum WK {
+    W_EMB, W_HEAD, W_LN0W, W_LN0B, W_LNOW, W_LNOB,
+    L_LN1W, L_LN1B, L_LN2W, L_LN2B,
+    L_XR, L_XW, L_XK, L_XV, L_XA, L_XG,
+    L_W0, L_W1, L_W2, L_A0, L_A1, L_A2, L_V0, L_V1, L_V2, L_G1, L_G2,
+    L_KK, L_KA, L_RK, L_WR, L_WK, L_WV, L_WO, L_LNXW, L_LNXB,
+    L_FXK, L_FK, L_FV, W_COUNT
+};
+constexpr int FIRST_LAYER_KIND = L_LN1W;
+
+const char *kind_name[W_COUNT] = {
+    "emb", "head", "ln0.w", "ln0.b", "ln_out.w", "ln_out.b",
+    "ln1.w", "ln1.b", "ln2.w", "ln2.b",
+    "att.x_r", "att.x_w", "att.x_k", "att.x_v", "att.x_a", "att.x_g",
+    "att.w0", "att.w1", "att.w2", "att.a0", "att.a1", "att.a2", "att.v0", "att.v1", "att.v2", "att.g1", "att.g2",
+    "att.k_k", "att.k_a", "att.r_k", "att.receptance", "att.key", "att.value", "att.output", "att.ln_x.w",
+    "att.ln_x.b", "ffn.x_k", "ffn.key", "ffn.value"};
+
+// kernel classes reported by rwkv7_profile_step
+enum PClass { P_EMBED, P_LN_MIX, P_GEMM_PROJ, P_GEMM_LORA, P_WKV, P_GEMM_OUT, P_GEMM_KEY, P_GEMM_VALUE, P_LN_OUT,
+              P_GEMM_HEAD, P_SAMPLER, P_COUNT };
+
+struct Prof {
+    std::vector<cudaEvent_t> ev;  // pairs (begin, end)
+    std::vector<int> cls;
+    size_t n = 0;
+};
+
+// activation buffers addressed by tensor maps
+enum ABuf { A_XR, A_XW, A_XK, A_XV, A_XA, A_XG, A_HW, A_HA, A_HV, A_HG, A_Z, A_XKF, A_H, A_XO, A_COUNT };
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+}  // namespace
+
+struct rwkv7_ctx {
+    rwkv7_config cfg{};
+    int L = 0, d = 0, H = 0, F = 0, V = 0, rw = 0, ra = 0, rv = 0, rg = 0, n_slots = 0;
+    int bcap = 0;  // activation rows (max slots per fused step, rounded up to 16)
+    int nsm = 0;
+    cudaStream_t stream = nullptr;
+    int mode = 0;
+    std::string err;
+
+    // weights
+    int wrows[W_COUNT]{}, wcols[W_COUNT]{};
+    __half *w[W_COUNT]{};
+    std::vector<uint8_t> wset;  // [W_COUNT][L] (globals use index 0)
+    size_t n_missing = 0;
+
+    // slot pool
+    float *wkv = nullptr, *shift_att = nullptr, *shift_ffn = nullptr, *occ = nullptr;
+    SampleParamsDev *params = nullptr;
+    unsigned long long *ndraw = nullptr;
+
+    // activations
+    __half *xmix[6]{};
+    __half *hw = nullptr, *ha = nullptr, *hv = nullptr, *hg = nullptr, *z = nullptr, *xk = nullptr, *h = nullptr,
+           *xo = nullptr;
+    float *r = nullptr, *k = nullptr, *v = nullptr, *dec = nullptr, *a = nullptr, *vg = nullptr, *g = nullptr,
+          *vfirst = nullptr, *x = nullptr, *logits = nullptr, *lpen = nullptr;
+    uint32_t *nz = nullptr;
+    int32_t *slots = nullptr, *tokens = nullptr, *next = nullptr;
+    float *ws = nullptr;
+    uint32_t *counters = nullptr;
+    uint32_t *errw = nullptr;
+    size_t ws_floats = 0;
+
+    CUtensorMap wmap[W_COUNT]{};
+    bool has_wmap[W_COUNT]{};
+    CUtensorMap amap[A_COUNT]{};
+
+    std::map<std::tuple<int, int, int, int>, cudaGraphExec_t> graphs;
+    std::vector<void *> allocs;
+    Prof prof;
+};
+
+namespace {
+
+int fail(rwkv7_ctx *c, int code, const char *fmt, ...) {
+    if (c) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        c->err = buf;
+    }
+    return code;
+}
+
+#define CK(call)                                                                                   \
+    do {                                                                                           \
+        cudaError_t e_ = (call);                                                                   \
+        if (e_ != cudaSuccess) return fail(c, RWKV7_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+    } while (0)
+
+template <typename T>
+int dalloc(rwkv7_ctx *c, T **p, size_t count) {
+    void *q = nullptr;
+    cudaError_t e = cudaMalloc(&q, count * sizeof(T) + 256);
+    if (e != cudaSuccess) return fail(c, RWKV7_ENOMEM, "cudaMalloc(%zu bytes): %s", count * sizeof(T), cudaGetErrorString(e));
+    c->allocs.push_back(q);
+    e = cudaMemset(q, 0, count * sizeof(T) + 256);
+    if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "cudaMemset: %s", cudaGetErrorString(e));
+    *p = (T *)q;
+    return RWKV7_OK;
+}
+
+bool per_layer(int kind) { return kind >= FIRST_LAYER_KIND; }
+
+int make_map(rwkv7_ctx *c, CUtensorMap *m, void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
+             const uint32_t *box) {
+    auto fn = encode_fn();
+    if (!fn) return fail(c, RWKV7_ECUDA, "cuTensorMapEncodeTiled is not available");
+    cuuint64_t gd[3], gs[2];
+    cuuint32_t bx[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, base, gd, gs, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(c, RWKV7_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return RWKV7_OK;
+}
+
+// Weight map: 3D {cols (K), rows, layers}, box {64, 128, 1}.
+int make_wmap(rwkv7_ctx *c, int kind) {
+    const int layers = per_layer(kind) ? c->L : 1;
+    uint64_t dims[3] = {(uint64_t)c->wcols[kind], (uint64_t)c->wrows[kind], (uint64_t)layers};
+    uint64_t strides[2] = {(uint64_t)c->wcols[kind] * 2, (uint64_t)c->wcols[kind] * c->wrows[kind] * 2};
+    uint32_t box[3] = {64, 128, 1};
+    c->has_wmap[kind] = true;
+    return make_map(c, &c->wmap[kind], c->w[kind], 3, dims, strides, box);
+}
+
+// Activation map: 2D {cols (K), bcap rows}, box {64, 16}.
+int make_amap(rwkv7_ctx *c, int which, void *base, int cols) {
+    uint64_t dims[2] = {(uint64_t)cols, (uint64_t)c->bcap};
+    uint64_t strides[1] = {(uint64_t)cols * 2};
+    uint32_t box[2] = {64, 16};
+    return make_map(c, &c->amap[which], base, 2, dims, strides, box);
+}
+
+// ---------------------------------------------------------------- GEMM launches
+struct Seg {
+    int wkind;    // weight kind
+    int xbuf;     // activation buffer
+    const __half *xptr;
+    int K;
+    int epi;
+    void *out;
+    int ldo;
+    const __half *bias;
+};
+
+int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *nz_out, const uint32_t *nz_skip,
+             const LaunchCfg &lc, int mode) {
+    GemmParams p;
+    memset(&p, 0, sizeof p);
+    int nmaps = 0;
+    int wslot[W_COUNT], aslot[A_COUNT];
+    for (int i = 0; i < W_COUNT; ++i) wslot[i] = -1;
+    for (int i = 0; i < A_COUNT; ++i) aslot[i] = -1;
+    int tile = 0, unit = 0, blk = 0;
+    for (int s = 0; s < n; ++s) {
+        const Seg &sg = segs[s];
+        GemmSeg &g = p.seg[s];
+        const int rows = c->wrows[sg.wkind];
+        if (wslot[sg.wkind] < 0) {
+            if (nmaps >= GEMM_MAX_MAPS) return fail(c, RWKV7_ECUDA, "too many tensor maps in one GEMM");
+            wslot[sg.wkind] = nmaps;
+            p.maps[nmaps++] = c->wmap[sg.wkind];
+        }
+        if (aslot[sg.xbuf] < 0) {
+            if (nmaps >= GEMM_MAX_MAPS) return fail(c, RWKV7_ECUDA, "too many tensor maps in one GEMM");
+            aslot[sg.xbuf] = nmaps;
+            p.maps[nmaps++] = c->amap[sg.xbuf];
+        }
+        g.wmap = wslot[sg.wkind];
+        g.xmap = aslot[sg.xbuf];
+        g.layer = per_layer(sg.wkind) ? layer : 0;
+        g.rows = rows;
+        g.K = sg.K;
+        g.kb = (sg.K + GEMM_TILE_K - 1) / GEMM_TILE_K;
+        g.epi = sg.epi;
+        g.out = sg.out;
+        g.ldo = sg.ldo;
+        g.bias = sg.bias;
+        g.w = c->w[sg.wkind] + (size_t)g.layer * rows * sg.K;
+        g.x = sg.xptr;
+        g.ldx = sg.K;
+        if (mode == 2) {
+            g.tile0 = blk;
+            blk += (rows + 63) / 64;
+        } else {
+            g.tile0 = tile;
+            g.unit0 = unit;
+            const int tiles = (rows + GEMM_TILE_M - 1) / GEMM_TILE_M;
+            tile += tiles;
+            unit += tiles * g.kb;
+        }
+    }
+    p.nseg = n;
+    p.nmaps = nmaps;
+    p.ntiles = tile;
+    p.nunits = unit;
+    p.B = B;
+    p.npad = (B + 15) / 16 * 16;
+    p.nz_out = nz_out;
+    p.nz_skip = nz_skip;
+    p.ws = c->ws;
+    p.counters = c->counters;
+    p.err = c->errw;
+    cudaError_t e = cudaSuccess;
+    if (mode == 2) {
+        launch_gemm_simt(p, lc, &e);
+    } else {
+        // one CTA per SM; a small pipeline leaves room for the next kernel's CTA
+        const size_t stage = 16384 + (size_t)p.npad * 128;
+        int stages;
+        if (p.npad <= 64)
+            stages = (int)std::min<size_t>(6, (112 * 1024 - 2048) / stage);
+        else
+            stages = (int)std::min<size_t>(8, (220 * 1024 - 2048) / stage);
+        if (stages < 2) stages = 2;
+        p.stages = stages;
+        p.prefetch = nz_skip == nullptr ? 1 : 0;
+        int grid = std::min(p.nunits, c->nsm);
+        if ((size_t)grid * 2 * p.npad * GEMM_TILE_M > c->ws_floats) return fail(c, RWKV7_ECUDA, "workspace too small");
+        if (p.ntiles > 4096) return fail(c, RWKV7_ECUDA, "too many tiles");
+        launch_gemm_tc(p, grid, gemm_tc_smem_bytes(p.npad, stages), lc, &e);
+    }
+    if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return RWKV7_OK;
+}
+
+const __half *LW(rwkv7_ctx *c, int kind, int l) {
+    return c->w[kind] + (size_t)l * c->wrows[kind] * c->wcols[kind];
+}
+
+// Enqueue one fused step for rows [0, B) of the activation buffers (slots and
+// tokens already in c->slots / c->tokens).
+int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf = nullptr) {
+    LaunchCfg lc{c->stream, mode != 2 && pf == nullptr};
+    LaunchCfg lc0{c->stream, false};
+    cudaError_t e = cudaSuccess;
+    // optional CUDA-event bracketing of every launch (profiling mode only)
+    auto pb = [&](int cls) {
+        if (!pf) return;
+        if (pf->n + 2 > pf->ev.size()) {
+            for (int i = 0; i < 64; ++i) {
+                cudaEvent_t ev;
+                cudaEventCreate(&ev);
+                pf->ev.push_back(ev);
+            }
+        }
+        pf->cls.push_back(cls);
+        cudaEventRecord(pf->ev[pf->n++], c->stream);
+    };
+    auto pe = [&]() {
+        if (pf) cudaEventRecord(pf->ev[pf->n++], c->stream);
+    };
+    const int d = c->d;
+    ElemParams ep;
+    memset(&ep, 0, sizeof ep);
+    ep.B = B;
+    ep.d = d;
+    ep.H = c->H;
+    ep.F = c->F;
+    ep.V = c->V;
+    ep.n_slots = c->n_slots;
+    ep.L = c->L;
+    ep.slots = c->slots;
+    ep.tokens = c->tokens;
+    ep.x = c->x;
+    ep.err = c->errw;
+    ep.emb = c->w[W_EMB];
+    ep.ln_w = c->w[W_LN0W];
+    ep.ln_b = c->w[W_LN0B];
+    pb(P_EMBED);
+    launch_embed(ep, lc0, &e);
+    pe();
+    if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "embed launch: %s", cudaGetErrorString(e));
+    int rc;
+    for (int l = 0; l < c->L; ++l) {
+        // LN1 + token shift + 6 mixes
+        ElemParams m = ep;
+        m.layer = l;
+        m.ln_w = LW(c, L_LN1W, l);
+        m.ln_b = LW(c, L_LN1B, l);
+        const int mk[6] = {L_XR, L_XW, L_XK, L_XV, L_XA, L_XG};
+        for (int q = 0; q < 6; ++q) {
+            m.mu[q] = LW(c, mk[q], l);
+            m.xo[q] = c->xmix[q];
+        }
+        m.shift = c->shift_att + (size_t)l * c->n_slots * d;
+        pb(P_LN_MIX);
+        launch_ln_mix(m, 6, lc, &e);
+        pe();
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
+        // G1: r, k, v and the LoRA down projections
+        Seg g1[7];
+        int n1 = 0;
+        g1[n1++] = {L_WR, A_XR, c->xmix[0], d, EPI_F32, c->r, d, nullptr};
+        g1[n1++] = {L_WK, A_XK, c->xmix[2], d, EPI_F32, c->k, d, nullptr};
+        g1[n1++] = {L_WV, A_XV, c->xmix[3], d, EPI_F32, c->v, d, nullptr};
+        g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F16_TANH, c->hw, c->rw, nullptr};
+        g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F16, c->ha, c->ra, nullptr};
+        if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F16, c->hv, c->rv, nullptr};
+        g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F16_SIGMOID, c->hg, c->rg, nullptr};
+        pb(P_GEMM_PROJ);
+        if ((rc = run_gemm(c, l, g1, n1, B, nullptr, nullptr, lc, mode))) return rc;
+        pe();
+        // G2: LoRA up projections with their gates
+        Seg g2[4];
+        int n2 = 0;
+        g2[n2++] = {L_W2, A_HW, c->hw, c->rw, EPI_DECAY, c->dec, d, LW(c, L_W0, l)};
+        g2[n2++] = {L_A2, A_HA, c->ha, c->ra, EPI_SIGMOID_BIAS, c->a, d, LW(c, L_A0, l)};
+        if (l > 0) g2[n2++] = {L_V2, A_HV, c->hv, c->rv, EPI_SIGMOID_BIAS, c->vg, d, LW(c, L_V0, l)};
+        g2[n2++] = {L_G2, A_HG, c->hg, c->rg, EPI_F32, c->g, d, nullptr};
+        pb(P_GEMM_LORA);
+        if ((rc = run_gemm(c, l, g2, n2, B, nullptr, nullptr, lc, mode))) return rc;
+        pe();
+        // WKV7 + GroupNorm + bonus + gate
+        WkvParams wp;
+        memset(&wp, 0, sizeof wp);
+        wp.B = B;
+        wp.d = d;
+        wp.H = c->H;
+        wp.n_slots = c->n_slots;
+        wp.layer = l;
+        wp.slots = c->slots;
+        wp.r = c->r;
+        wp.k = c->k;
+        wp.v = c->v;
+        wp.dec = c->dec;
+        wp.a = c->a;
+        wp.vg = c->vg;
+        wp.g = c->g;
+        wp.v_first = c->vfirst;
+        wp.k_k = LW(c, L_KK, l);
+        wp.k_a = LW(c, L_KA, l);
+        wp.r_k = LW(c, L_RK, l);
+        wp.lnx_w = LW(c, L_LNXW, l);
+        wp.lnx_b = LW(c, L_LNXB, l);
+        wp.wkv = c->wkv + (size_t)l * c->n_slots * c->H * HS * HS;
+        wp.z = c->z;
+        wp.err = c->errw;
+        pb(P_WKV);
+        launch_wkv(wp, lc, &e);
+        pe();
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "wkv launch: %s", cudaGetErrorString(e));
+        // G3: output projection into the residual
+        Seg g3[1] = {{L_WO, A_Z, c->z, d, EPI_RESID, c->x, d, nullptr}};
+        pb(P_GEMM_OUT);
+        if ((rc = run_gemm(c, l, g3, 1, B, nullptr, nullptr, lc, mode))) return rc;
+        pe();
+        // LN2 + token shift + mix
+        ElemParams m2 = ep;
+        m2.layer = l;
+        m2.ln_w = LW(c, L_LN2W, l);
+        m2.ln_b = LW(c, L_LN2B, l);
+        m2.mu[0] = LW(c, L_FXK, l);
+        m2.xo[0] = c->xk;
+        m2.shift = c->shift_ffn + (size_t)l * c->n_slots * d;
+        pb(P_LN_MIX);
+        launch_ln_mix(m2, 1, lc, &e);
+        pe();
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
+        // G4: key + ReLU^2 (+ nonzero flags per 64 hidden units)
+        Seg g4[1] = {{L_FK, A_XKF, c->xk, d, EPI_RELU2, c->h, c->F, nullptr}};
+        pb(P_GEMM_KEY);
+        if ((rc = run_gemm(c, l, g4, 1, B, c->nz, nullptr, lc, mode))) return rc;
+        pe();
+        // G5: value over the nonzero hidden blocks, into the residual
+        Seg g5[1] = {{L_FV, A_H, c->h, c->F, EPI_RESID, c->x, d, nullptr}};
+        pb(P_GEMM_VALUE);
+        if ((rc = run_gemm(c, l, g5, 1, B, nullptr, c->nz, lc, mode))) return rc;
+        pe();
+    }
+    if (head) {
+        ElemParams o = ep;
+        o.ln_w = c->w[W_LNOW];
+        o.ln_b = c->w[W_LNOB];
+        o.xo[0] = c->xo;
+        pb(P_LN_OUT);
+        launch_ln_out(o, lc, &e);
+        pe();
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_out launch: %s", cudaGetErrorString(e));
+        Seg gh[1] = {{W_HEAD, A_XO, c->xo, d, EPI_F32, c->logits, c->V, nullptr}};
+        pb(P_GEMM_HEAD);
+        if ((rc = run_gemm(c, 0, gh, 1, B, nullptr, nullptr, lc, mode))) return rc;
+        pe();
+        if (sample) {
+            SamplerParams sp;
+            memset(&sp, 0, sizeof sp);
+            sp.B = B;
+            sp.V = c->V;
+            sp.n_slots = c->n_slots;
+            sp.slots = c->slots;
+            sp.logits = c->logits;
+            sp.occ = c->occ;
+            sp.params = c->params;
+            sp.ndraw = c->ndraw;
+            sp.lpen = c->lpen;
+            sp.next = c->next;
+            sp.err = c->errw;
+            pb(P_SAMPLER);
+            launch_sampler(sp, lc, &e);
+            pe();
+            if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "sampler launch: %s", cudaGetErrorString(e));
+        }
+    }
+    return RWKV7_OK;
+}
+
+int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
+    if (c->mode != 0) return enqueue_step(c, B, head, sample, c->mode);
+    auto key = std::make_tuple(B, (int)head, (int)sample, c->mode);
+    auto it = c->graphs.find(key);
+    if (it == c->graphs.end()) {
+        cudaGraph_t g = nullptr;
+        CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+        int rc = enqueue_step(c, B, head, sample, 0);
+        cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+        if (rc) {
+            if (g) cudaGraphDestroy(g);
+            return rc;
+        }
+        if (e2 != cudaSuccess) return fail(c, RWKV7_ECUDA, "graph capture: %s", cudaGetErrorString(e2));
+        cudaGraphExec_t ex = nullptr;
+        cudaError_t e3 = cudaGraphInstantiate(&ex, g, 0);
+        cudaGraphDestroy(g);
+        if (e3 != cudaSuccess) return fail(c, RWKV7_ECUDA, "graph instantiate: %s", cudaGetErrorString(e3));
+        it = c->graphs.emplace(key, ex).first;
+    }
+    CK(cudaGraphLaunch(it->second, c->stream));
+    return RWKV7_OK;
+}
+
+__global__ void set_i32_kernel(int32_t *p, int32_t v) { *p = v; }
+
+int check_ready(rwkv7_ctx *c) {
+    if (c->n_missing) return fail(c, RWKV7_ESTATE, "%zu weight tensors have not been set", c->n_missing);
+    return RWKV7_OK;
+}
+
+int parse_name(rwkv7_ctx *c, const char *name, int *kind, int *layer) {
+    *layer = 0;
+    const char *rest = name;
+    if (strncmp(name, "blocks.", 7) == 0) {
+        char *end = nullptr;
+        long l = strtol(name + 7, &end, 10);
+        if (end == name + 7 || *end != '.' || l < 0 || l >= c->L) return -1;
+        *layer = (int)l;
+        rest = end + 1;
+        for (int k = FIRST_LAYER_KIND; k < W_COUNT; ++k)
+            if (strcmp(rest, kind_name[k]) == 0) {
+                *kind = k;
+                return 0;
+            }
+        return -1;
+    }
+    for (int k = 0; k < FIRST_LAYER_KIND; ++k)
+        if (strcmp(rest, kind_name[k]) == 0) {
+            *kind = k;
+            return 0;
+        }
+    return -1;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
+    if (!cfg || !out) return RWKV7_EINVAL;
+    *out = nullptr;
+    const rwkv7_config &g = *cfg;
+    if (g.head_size != HS || g.n_layer < 1 || g.d_model < HS || g.d_model % HS || g.d_model > 8192 ||
+        g.d_ffn < 64 || g.d_ffn % 64 || g.vocab < 1 || g.n_slots < 1 || g.n_slots > 65536)
+        return RWKV7_EINVAL;
+    for (int r : {g.lora_w, g.lora_a, g.lora_v, g.lora_g})
+        if (r < 8 || r % 8) return RWKV7_EINVAL;
+    if (g.vocab % 8) return RWKV7_EINVAL;
+    rwkv7_ctx *c = new rwkv7_ctx();
+    c->cfg = g;
+    c->L = g.n_layer;
+    c->d = g.d_model;
+    c->H = g.d_model / HS;
+    c->F = g.d_ffn;
+    c->V = g.vocab;
+    c->rw = g.lora_w;
+    c->ra = g.lora_a;
+    c->rv = g.lora_v;
+    c->rg = g.lora_g;
+    c->n_slots = g.n_slots;
+    c->bcap = (std::min(g.n_slots, MAX_B) + 15) / 16 * 16;
+    c->stream = (cudaStream_t)cuda_stream;
+    int dev = 0;
+    int rc = RWKV7_OK;
+    auto bad = [&](int code) {
+        *out = c;  // keep the ctx so the caller can read the error, then destroy it
+        return code;
+    };
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return bad(fail(c, RWKV7_ECUDA, "no CUDA device"));
+    const int d = c->d, F = c->F, V = c->V, L = c->L;
+    auto shp = [&](int k, int rows, int cols) {
+        c->wrows[k] = rows;
+        c->wcols[k] = cols;
+    };
+    shp(W_EMB, V, d); shp(W_HEAD, V, d);
+    shp(W_LN0W, 1, d); shp(W_LN0B, 1, d); shp(W_LNOW, 1, d); shp(W_LNOB, 1, d);
+    for (int k : {L_LN1W, L_LN1B, L_LN2W, L_LN2B, L_XR, L_XW, L_XK, L_XV, L_XA, L_XG, L_W0, L_A0, L_V0, L_KK, L_KA,
+                  L_RK, L_LNXW, L_LNXB, L_FXK})
+        shp(k, 1, d);
+    shp(L_W1, c->rw, d); shp(L_W2, d, c->rw);
+    shp(L_A1, c->ra, d); shp(L_A2, d, c->ra);
+    shp(L_V1, c->rv, d); shp(L_V2, d, c->rv);
+    shp(L_G1, c->rg, d); shp(L_G2, d, c->rg);
+    shp(L_WR, d, d); shp(L_WK, d, d); shp(L_WV, d, d); shp(L_WO, d, d);
+    shp(L_FK, F, d); shp(L_FV, d, F);
+    c->wset.assign((size_t)W_COUNT * L, 0);
+    for (int k = 0; k < W_COUNT; ++k) {
+        const size_t layers = per_layer(k) ? L : 1;
+        if ((rc = dalloc(c, &c->w[k], layers * c->wrows[k] * c->wcols[k]))) return bad(rc);
+        c->n_missing += layers;
+    }
+    static const int tc_kinds[] = {L_WR, L_WK, L_WV, L_W1, L_A1, L_V1, L_G1, L_W2, L_A2, L_V2, L_G2, L_WO, L_FK, L_FV, W_HEAD};
+    for (int k : tc_kinds)
+        if ((rc = make_wmap(c, k))) return bad(rc);
+    const size_t ns = c->n_slots;
+    if ((rc = dalloc(c, &c->wkv, (size_t)L * ns * c->H * HS * HS))) return bad(rc);
+    if ((rc = dalloc(c, &c->shift_att, (size_t)L * ns * d))) return bad(rc);
+    if ((rc = dalloc(c, &c->shift_ffn, (size_t)L * ns * d))) return bad(rc);
+    if ((rc = dalloc(c, &c->occ, ns * V))) return bad(rc);
+    if ((rc = dalloc(c, &c->params, ns))) return bad(rc);
+    if ((rc = dalloc(c, &c->ndraw, ns))) return bad(rc);
+    {
+        std::vector<SampleParamsDev> def(ns);
+        for (auto &p : def) {
+            p.temperature = 1.0f;
+            p.top_p = 0.3f;
+            p.top_k = 0;
+            p.presence = 0.0f;
+            p.frequency = 1.0f;
+            p.penalty_decay = 0.996f;
+            p.seed = 0;
+            p.greedy = 0;
+            p.pad = 0;
+        }
+        if (cudaMemcpy(c->params, def.data(), ns * sizeof(SampleParamsDev), cudaMemcpyHostToDevice) != cudaSuccess)
+            return bad(fail(c, RWKV7_ECUDA, "params upload"));
+    }
+    const size_t R = c->bcap;
+    for (int q = 0; q < 6; ++q)
+        if ((rc = dalloc(c, &c->xmix[q], R * d))) return bad(rc);
+    if ((rc = dalloc(c, &c->hw, R * c->rw)) || (rc = dalloc(c, &c->ha, R * c->ra)) ||
+        (rc = dalloc(c, &c->hv, R * c->rv)) || (rc = dalloc(c, &c->hg, R * c->rg)) || (rc = dalloc(c, &c->z, R * d)) ||
+        (rc = dalloc(c, &c->xk, R * d)) || (rc = dalloc(c, &c->h, R * F)) || (rc = dalloc(c, &c->xo, R * d)))
+        return bad(rc);
+    if ((rc = dalloc(c, &c->r, R * d)) || (rc = dalloc(c, &c->k, R * d)) || (rc = dalloc(c, &c->v, R * d)) ||
+        (rc = dalloc(c, &c->dec, R * d)) || (rc = dalloc(c, &c->a, R * d)) || (rc = dalloc(c, &c->vg, R * d)) ||
+        (rc = dalloc(c, &c->g, R * d)) || (rc = dalloc(c, &c->vfirst, R * d)) || (rc = dalloc(c, &c->x, R * d)) ||
+        (rc = dalloc(c, &c->logits, R * V)) || (rc = dalloc(c, &c->lpen, R * V)))
+        return bad(rc);
+    if ((rc = dalloc(c, &c->nz, (size_t)F / 64 + 64))) return bad(rc);
+    if ((rc = dalloc(c, &c->slots, R)) || (rc = dalloc(c, &c->tokens, R)) || (rc = dalloc(c, &c->next, R)))
+        return bad(rc);
+    c->ws_floats = (size_t)c->nsm * 2 * R * GEMM_TILE_M;
+    if ((rc = dalloc(c, &c->ws, c->ws_floats))) return bad(rc);
+    if ((rc = dalloc(c, &c->counters, 4096))) return bad(rc);
+    if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
+    const int mk[6] = {A_XR, A_XW, A_XK, A_XV, A_XA, A_XG};
+    for (int q = 0; q < 6; ++q)
+        if ((rc = make_amap(c, mk[q], c->xmix[q], d))) return bad(rc);
+    if ((rc = make_amap(c, A_HW, c->hw, c->rw)) || (rc = make_amap(c, A_HA, c->ha, c->ra)) ||
+        (rc = make_amap(c, A_HV, c->hv, c->rv)) || (rc = make_amap(c, A_HG, c->hg, c->rg)) ||
+        (rc = make_amap(c, A_Z, c->z, d)) || (rc = make_amap(c, A_XKF, c->xk, d)) ||
+        (rc = make_amap(c, A_H, c->h, F)) || (rc = make_amap(c, A_XO, c->xo, d)))
+        return bad(rc);
+    if (cudaDeviceSynchronize() != cudaSuccess) return bad(fail(c, RWKV7_ECUDA, "device sync after create"));
+    *out = c;
+    return RWKV7_OK;
+}
+
+void rwkv7_destroy(rwkv7_ctx *c) {
+    if (!c) return;
+    cudaStreamSynchronize(c->stream);
+    for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second);
+    for (cudaEvent_t ev : c->prof.ev) cudaEventDestroy(ev);
+    for (void *p : c->allocs) cudaFree(p);
+    delete c;
+}
+
+const char *rwkv7_last_error(const rwkv7_ctx *c) { return c ? c->err.c_str() : "null context"; }
+
+int rwkv7_set_weight(rwkv7_ctx *c, const char *name, const void *host_f16, size_t bytes) {
+    if (!c) return RWKV7_EINVAL;
+    if (!name || !host_f16) return fail(c, RWKV7_EINVAL, "null argument");
+    int kind, layer;
+    if (parse_name(c, name, &kind, &layer)) return fail(c, RWKV7_ESHAPE, "unknown weight name '%s'", name);
+    const size_t n = (size_t)c->wrows[kind] * c->wcols[kind];
+    if (bytes != n * 2) return fail(c, RWKV7_ESHAPE, "'%s': %zu bytes given, %zu expected", name, bytes, n * 2);
+    CK(cudaMemcpy(c->w[kind] + (size_t)layer * n, host_f16, bytes, cudaMemcpyHostToDevice));
+    uint8_t &f = c->wset[(size_t)kind * c->L + layer];
+    if (!f) {
+        f = 1;
+        c->n_missing--;
+    }
+    return RWKV7_OK;
+}
+
+int rwkv7_load_weights(rwkv7_ctx *c, const char *path) {
+    if (!c) return RWKV7_EINVAL;
+    if (!path) return fail(c, RWKV7_EINVAL, "null path");
+    FILE *fh = fopen(path, "rb");
+    if (!fh) return fail(c, RWKV7_EINVAL, "cannot open '%s'", path);
+    std::vector<char> head(4096 + 1, 0);
+    if (fread(head.data(), 1, 4096, fh) != 4096 || strncmp(head.data(), "RWKV7W01\n", 9) != 0) {
+        fclose(fh);
+        return fail(c, RWKV7_ESHAPE, "'%s' is not an RWKV7W01 weight file", path);
+    }
+    const char *p = head.data() + 9;
+    int n = atoi(p);
+    p = strchr(p, '\n');
+    int rc = RWKV7_OK;
+    std::vector<uint8_t> buf;
+    for (int i = 0; i < n && p && rc == RWKV7_OK; ++i) {
+        ++p;
+        char name[256], dt[16], shape[64];
+        unsigned long long off = 0, nb = 0;
+        if (sscanf(p, "%255s %15s %63s %llu %llu", name, dt, shape, &off, &nb) != 5 || strcmp(dt, "f16") != 0) {
+            rc = fail(c, RWKV7_ESHAPE, "bad header line %d in '%s'", i, path);
+            break;
+        }
+        buf.resize(nb);
+        if (fseek(fh, (long)(4096 + off), SEEK_SET) != 0 || fread(buf.data(), 1, nb, fh) != nb) {
+            rc = fail(c, RWKV7_ESHAPE, "short read of '%s' in '%s'", name, path);
+            break;
+        }
+        rc = rwkv7_set_weight(c, name, buf.data(), nb);
+        p = strchr(p, '\n');
+    }
+    fclose(fh);
+    return rc;
+}
+
+static int slot_op(rwkv7_ctx *c, int op, int a, int b) {
+    SlotOpParams p;
+    memset(&p, 0, sizeof p);
+    p.op = op;
+    p.a = a;
+    p.b = b;
+    p.L = c->L;
+    p.n_slots = c->n_slots;
+    p.wkv_per_slot = (size_t)c->H * HS * HS;
+    p.d = c->d;
+    p.V = c->V;
+    p.wkv = c->wkv;
+    p.shift_att = c->shift_att;
+    p.shift_ffn = c->shift_ffn;
+    p.occ = c->occ;
+    p.ndraw = c->ndraw;
+    p.params = c->params;
+    cudaError_t e = cudaSuccess;
+    launch_slot_op(p, c->stream, &e);
+    if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "slot op: %s", cudaGetErrorString(e));
+    return RWKV7_OK;
+}
+
+#define SLOT_OK(s) ((s) >= 0 && (s) < c->n_slots)
+
+int rwkv7_slot_reset(rwkv7_ctx *c, int32_t slot) {
+    if (!c) return RWKV7_EINVAL;
+    if (!SLOT_OK(slot)) return fail(c, RWKV7_EINVAL, "slot %d out of range", slot);
+    return slot_op(c, 0, slot, slot);
+}
+
+int rwkv7_slot_swap(rwkv7_ctx *c, int32_t a, int32_t b) {
+    if (!c) return RWKV7_EINVAL;
+    if (!SLOT_OK(a) || !SLOT_OK(b)) return fail(c, RWKV7_EINVAL, "slot out of range");
+    if (a == b) return RWKV7_OK;
+    return slot_op(c, 2, a, b);
+}
+
+int rwkv7_slot_copy(rwkv7_ctx *c, int32_t src, int32_t dst) {
+    if (!c) return RWKV7_EINVAL;
+    if (!SLOT_OK(src) || !SLOT_OK(dst)) return fail(c, RWKV7_EINVAL, "slot out of range");
+    if (src == dst) return RWKV7_OK;
+    return slot_op(c, 1, src, dst);
+}
+
+int rwkv7_slot_set_sampling(rwkv7_ctx *c, int32_t slot, const rwkv7_sampling *sp) {
+    if (!c) return RWKV7_EINVAL;
+    if (!SLOT_OK(slot) || !sp) return fail(c, RWKV7_EINVAL, "bad slot or null params");
+    if (!(sp->top_p >= 0.0f) || sp->top_k < 0 || !(sp->penalty_decay >= 0.0f))
+        return fail(c, RWKV7_EINVAL, "invalid sampling parameters");
+    SampleParamsDev d;
+    d.temperature = sp->temperature;
+    d.top_p = sp->top_p;
+    d.top_k = sp->top_k;
+    d.presence = sp->presence;
+    d.frequency = sp->frequency;
+    d.penalty_decay = sp->penalty_decay;
+    d.seed = sp->seed;
+    d.greedy = sp->greedy;
+    d.pad = 0;
+    CK(cudaMemcpyAsync(c->params + slot, &d, sizeof d, cudaMemcpyHostToDevice, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    return RWKV7_OK;
+}
+
+size_t rwkv7_slot_state_bytes(const rwkv7_ctx *c) {
+    if (!c) return 0;
+    return ((size_t)c->L * c->H * HS * HS + 2 * (size_t)c->L * c->d) * sizeof(float);
+}
+
+static int state_xfer(rwkv7_ctx *c, int32_t slot, void *host, size_t bytes, bool to_host) {
+    if (!SLOT_OK(slot) || !host) return fail(c, RWKV7_EINVAL, "bad slot or null buffer");
+    if (bytes != rwkv7_slot_state_bytes(c)) return fail(c, RWKV7_EINVAL, "state buffer must be %zu bytes", rwkv7_slot_state_bytes(c));
+    CK(cudaStreamSynchronize(c->stream));
+    const size_t per = (size_t)c->H * HS * HS;
+    char *hp = (char *)host;
+    for (int l = 0; l < c->L; ++l) {
+        float *dp = c->wkv + ((size_t)l * c->n_slots + slot) * per;
+        if (to_host)
+            CK(cudaMemcpy(hp, dp, per * 4, cudaMemcpyDeviceToHost));
+        else
+            CK(cudaMemcpy(dp, hp, per * 4, cudaMemcpyHostToDevice));
+        hp += per * 4;
+    }
+    float *bases[2] = {c->shift_att, c->shift_ffn};
+    for (float *base : bases)
+        for (int l = 0; l < c->L; ++l) {
+            float *dp = base + ((size_t)l * c->n_slots + slot) * c->d;
+            if (to_host)
+                CK(cudaMemcpy(hp, dp, (size_t)c->d * 4, cudaMemcpyDeviceToHost));
+            else
+                CK(cudaMemcpy(dp, hp, (size_t)c->d * 4, cudaMemcpyHostToDevice));
+            hp += (size_t)c->d * 4;
+        }
+    return RWKV7_OK;
+}
+
+int rwkv7_slot_get_state(rwkv7_ctx *c, int32_t slot, void *host_buf, size_t bytes) {
+    if (!c) return RWKV7_EINVAL;
+    return state_xfer(c, slot, host_buf, bytes, true);
+}
+
+int rwkv7_slot_set_state(rwkv7_ctx *c, int32_t slot, const void *host_buf, size_t bytes) {
+    if (!c) return RWKV7_EINVAL;
+    return state_xfer(c, slot, (void *)host_buf, bytes, false);
+}
+
+int rwkv7_prefill_seq(rwkv7_ctx *c, int32_t slot, const int32_t *d_tokens, int32_t T, float *d_logits_out) {
+    if (!c) return RWKV7_EINVAL;
+    if (!SLOT_OK(slot) || !d_tokens || T <= 0) return fail(c, RWKV7_EINVAL, "bad slot, token pointer or length");
+    int rc;
+    if ((rc = check_ready(c))) return rc;
+    set_i32_kernel<<<1, 1, 0, c->stream>>>(c->slots, slot);
+    CK(cudaGetLastError());
+    for (int t = 0; t < T; ++t) {
+        CK(cudaMemcpyAsync(c->tokens, d_tokens + t, 4, cudaMemcpyDeviceToDevice, c->stream));
+        const bool last = (t == T - 1) && d_logits_out;
+        if ((rc = run_step(c, 1, last, false))) return rc;
+    }
+    if (d_logits_out)
+        CK(cudaMemcpyAsync(d_logits_out, c->logits, (size_t)c->V * 4, cudaMemcpyDeviceToDevice, c->stream));
+    return RWKV7_OK;
+}
+
+int rwkv7_decode_step(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_tokens, int32_t B, float *d_logits_out,
+                      int32_t *d_next_out) {
+    if (!c) return RWKV7_EINVAL;
+    if (!d_slots || !d_tokens || B < 1 || B > c->n_slots)
+        return fail(c, RWKV7_EINVAL, "bad decode arguments (B=%d, n_slots=%d)", B, c->n_slots);
+    int rc;
+    if ((rc = check_ready(c))) return rc;
+    const bool head = d_logits_out || d_next_out;
+    for (int off = 0; off < B; off += MAX_B) {
+        const int bs = std::min(MAX_B, B - off);
+        if (d_slots + off != c->slots)
+            CK(cudaMemcpyAsync(c->slots, d_slots + off, (size_t)bs * 4, cudaMemcpyDeviceToDevice, c->stream));
+        if (d_tokens + off != c->tokens)
+            CK(cudaMemcpyAsync(c->tokens, d_tokens + off, (size_t)bs * 4, cudaMemcpyDeviceToDevice, c->stream));
+        if ((rc = run_step(c, bs, head, d_next_out != nullptr))) return rc;
+        if (d_logits_out && d_logits_out + (size_t)off * c->V != c->logits)
+            CK(cudaMemcpyAsync(d_logits_out + (size_t)off * c->V, c->logits, (size_t)bs * c->V * 4,
+                               cudaMemcpyDeviceToDevice, c->stream));
+        if (d_next_out && d_next_out + off != c->next)
+            CK(cudaMemcpyAsync(d_next_out + off, c->next, (size_t)bs * 4, cudaMemcpyDeviceToDevice, c->stream));
+    }
+    return RWKV7_OK;
+}
+
+int rwkv7_decode_step_host(rwkv7_ctx *c, const int32_t *h_slots, const int32_t *h_tokens, int32_t B,
+                           float *h_logits_out, int32_t *h_next_out) {
+    if (!c) return RWKV7_EINVAL;
+    if (!h_slots || !h_tokens || B < 1 || B > c->n_slots) return fail(c, RWKV7_EINVAL, "bad decode arguments");
+    std::vector<uint8_t> seen(c->n_slots, 0);
+    for (int b = 0; b < B; ++b) {
+        if (!SLOT_OK(h_slots[b])) return fail(c, RWKV7_EINVAL, "slot %d out of range", h_slots[b]);
+        if (seen[h_slots[b]]++) return fail(c, RWKV7_EINVAL, "slot %d repeated", h_slots[b]);
+        if (h_tokens[b] < 0 || h_tokens[b] >= c->V) return fail(c, RWKV7_EINVAL, "token %d out of range", h_tokens[b]);
+    }
+    int rc;
+    if ((rc = check_ready(c))) return rc;
+    const bool head = h_logits_out || h_next_out;
+    for (int off = 0; off < B; off += MAX_B) {
+        const int bs = std::min(MAX_B, B - off);
+        CK(cudaMemcpyAsync(c->slots, h_slots + off, (size_t)bs * 4, cudaMemcpyHostToDevice, c->stream));
+        CK(cudaMemcpyAsync(c->tokens, h_tokens + off, (size_t)bs * 4, cudaMemcpyHostToDevice, c->stream));
+        if ((rc = run_step(c, bs, head, h_next_out != nullptr))) return rc;
+        if (h_logits_out)
+            CK(cudaMemcpyAsync(h_logits_out + (size_t)off * c->V, c->logits, (size_t)bs * c->V * 4,
+                               cudaMemcpyDeviceToHost, c->stream));
+        if (h_next_out)
+            CK(cudaMemcpyAsync(h_next_out + off, c->next, (size_t)bs * 4, cudaMemcpyDeviceToHost, c->stream));
+    }
+    CK(cudaStreamSynchronize(c->stream));
+    return RWKV7_OK;
+}
+
+int rwkv7_sample_batch(rwkv7_ctx *c, const int32_t *d_slots, const float *d_logits, int32_t B, int32_t *d_next_out) {
+    if (!c) return RWKV7_EINVAL;
+    if (!d_slots || !d_logits || !d_next_out || B < 1 || B > c->n_slots)
+        return fail(c, RWKV7_EINVAL, "bad sampling arguments");
+    for (int off = 0; off < B; off += c->bcap) {
+        const int bs = std::min(c->bcap, B - off);
+        SamplerParams sp;
+        memset(&sp, 0, sizeof sp);
+        sp.B = bs;
+        sp.V = c->V;
+        sp.n_slots = c->n_slots;
+        sp.slots = d_slots + off;
+        sp.logits = d_logits + (size_t)off * c->V;
+        sp.occ = c->occ;
+        sp.params = c->params;
+        sp.ndraw = c->ndraw;
+        sp.lpen = c->lpen;
+        sp.next = d_next_out + off;
+        sp.err = c->errw;
+        cudaError_t e = cudaSuccess;
+        launch_sampler(sp, LaunchCfg{c->stream, false}, &e);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "sampler launch: %s", cudaGetErrorString(e));
+    }
+    return RWKV7_OK;
+}
+
+int rwkv7_synchronize(rwkv7_ctx *c) {
+    if (!c) return RWKV7_EINVAL;
+    CK(cudaStreamSynchronize(c->stream));
+    uint32_t w = 0;
+    CK(cudaMemcpy(&w, c->errw, 4, cudaMemcpyDeviceToHost));
+    if (w) {
+        CK(cudaMemset(c->errw, 0, 4));
+        if (w & ERR_TIMEOUT) return fail(c, RWKV7_ETIMEOUT, "a bounded wait inside a kernel gave up (flags 0x%x)", w);
+        return fail(c, RWKV7_EINVAL, "device-side argument error (flags 0x%x: %s%s%s%s)", w,
+                    (w & ERR_SLOT) ? "slot out of range " : "", (w & ERR_TOKEN) ? "token out of range " : "",
+                    (w & ERR_DUP) ? "repeated slot " : "", (w & ERR_CONFIG) ? "sampler found no token" : "");
+    }
+    return RWKV7_OK;
+}
+
+int rwkv7_set_mode(rwkv7_ctx *c, int32_t mode) {
+    if (!c) return RWKV7_EINVAL;
+    if (mode < 0 || mode > 2) return fail(c, RWKV7_EINVAL, "mode must be 0, 1 or 2");
+    c->mode = mode;
+    return RWKV7_OK;
+}
+
+int32_t rwkv7_step_kernel_count(const rwkv7_ctx *c, int32_t B, int32_t with_sampling) {
+    if (!c || B < 1) return 0;
+    const int sub = (B + MAX_B - 1) / MAX_B;
+    return sub * (1 + 8 * c->L + 2 + (with_sampling ? 1 : 0));
+}
+
+int rwkv7_profile_step(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_tokens, int32_t B,
+                       int32_t with_sampling, float *ms_out, int32_t *launches_out, int32_t n_classes) {
+    if (!c) return RWKV7_EINVAL;
+    if (!d_slots || !d_tokens || !ms_out || !launches_out || B < 1 || B > c->bcap || n_classes < P_COUNT)
+        return fail(c, RWKV7_EINVAL, "bad profiling arguments (B must be <= %d, n_classes >= %d)", c->bcap, (int)P_COUNT);
+    int rc;
+    if ((rc = check_ready(c))) return rc;
+    if (d_slots != c->slots) CK(cudaMemcpyAsync(c->slots, d_slots, (size_t)B * 4, cudaMemcpyDeviceToDevice, c->stream));
+    if (d_tokens != c->tokens)
+        CK(cudaMemcpyAsync(c->tokens, d_tokens, (size_t)B * 4, cudaMemcpyDeviceToDevice, c->stream));
+    Prof &pf = c->prof;
+    pf.n = 0;
+    pf.cls.clear();
+    const int mode = c->mode == 2 ? 2 : 1;
+    if ((rc = enqueue_step(c, B, true, with_sampling != 0, mode, &pf))) return rc;
+    CK(cudaStreamSynchronize(c->stream));
+    for (int i = 0; i < n_classes; ++i) {
+        ms_out[i] = 0.0f;
+        launches_out[i] = 0;
+    }
+    for (size_t i = 0; i < pf.cls.size(); ++i) {
+        float ms = 0.0f;
+        CK(cudaEventElapsedTime(&ms, pf.ev[2 * i], pf.ev[2 * i + 1]));
+        ms_out[pf.cls[i]] += ms;
+        launches_out[pf.cls[i]] += 1;
+    }
+    return RWKV7_OK;
+}
+
+int rwkv7_get_io_buffers(rwkv7_ctx *c, int32_t **d_slots, int32_t **d_tokens, float **d_logits, int32_t **d_next) {
+    if (!c) return RWKV7_EINVAL;
+    if (d_slots) *d_slots = c->slots;
+    if (d_tokens) *d_tokens = c->tokens;
+    if (d_logits) *d_logits = c->logits;
+    if (d_next) *d_next = c->next;
+    return RWKV7_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,382 @@
+// sampler.cu -- batched next-token sampling, one CTA (1024 threads) per slot row.
+//
+// What is sampled follows the Albatross worker loop (RWKV-Runner Albatross
+// article, "连续批处理Worker 主循环": presence / frequency penalties, then
+// sample_next_tokens_batch with per-slot temperature / top_p / top_k) and the
+// adapter's defaults and occurrence decay ("适配器Runner 与异步引擎之间的桥":
+// penalty_decay 0.996).  The draw is made exact and order-independent by
+// working on integer weights:
+//   l_i  = logit_i - ((occ_i > 0 ? presence : 0) + occ_i * frequency)
+//   q1_i = floor(2^24 * 2^((l_i - max l) * log2 e))            (fp32 steps, no contraction)
+//   top-p keeps q1_i >= tp, tp the largest value whose tail mass reaches
+//   ceil(top_p * sum q1), found exactly with a two-level (12 + 12 bit) radix
+//   histogram of weight sums; top-k keeps the first k in (q1 desc, index asc)
+//   qT_i = floor(2^24 * 2^((l_i - max l) / T * log2 e)) on the kept set
+//   r = floor(u * R / 2^64), u one Philox4x32-10 draw (Salmon et al., SC'11),
+//   token = first kept index whose running qT sum exceeds r; then
+//   occ *= penalty_decay, occ[token] += 1.
+// greedy: argmax of the raw logits, lowest index on ties.
+#include "internal.cuh"
+
+namespace rk {
+
+constexpr int SMP_THREADS = 1024;
+constexpr int NBUCKET = 4097;  // q1 >> 12 for q1 in [0, 2^24]
+
+// 2^e for e <= 0: e = n + f (n nearest integer, f exact), 2^f by its degree-7
+// Taylor polynomial in f ln 2 (coefficients (ln 2)^k / k!), Horner with fused
+// multiply-adds, then an exact scale by 2^n.
+__device__ __forceinline__ float exp2_own(float e) {
+    if (!(e > -126.0f)) return 0.0f;
+    if (e > 0.0f) e = 0.0f;
+    const float n = floorf(__fadd_rn(e, 0.5f));
+    const float f = __fsub_rn(e, n);
+    float z = 0.0000152527338040598403f;
+    z = __fmaf_rn(z, f, 0.000154035303933816099f);
+    z = __fmaf_rn(z, f, 0.00133335581464284434f);
+    z = __fmaf_rn(z, f, 0.00961812910762847717f);
+    z = __fmaf_rn(z, f, 0.0555041086648215800f);
+    z = __fmaf_rn(z, f, 0.240226506959100712f);
+    z = __fmaf_rn(z, f, 0.693147180559945309f);
+    z = __fmaf_rn(z, f, 1.0f);
+    const float sc = __int_as_float(((int)n + 127) << 23);
+    return __fmul_rn(z, sc);
+}
+
+__device__ __forceinline__ uint32_t qweight(float l, float m, float T) {
+    float dlt = __fsub_rn(l, m);
+    if (T != 1.0f) dlt = __fdiv_rn(dlt, T);
+    const float e = __fmul_rn(dlt, 1.44269504088896340736f);
+    const float pz = exp2_own(e);
+    return (uint32_t)floorf(__fmul_rn(pz, 16777216.0f));
+}
+
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c[0]), lo0 = 0xD2511F53u * c[0];
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c[2]), lo1 = 0xCD9E8D57u * c[2];
+        const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = lo1;
+        c[2] = n2;
+        c[3] = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+}
+
+struct SmpShared {
+    unsigned long long hist[NBUCKET];
+    unsigned long long wsum[32];
+    float wf[32];
+    int wi[32];
+    unsigned long long bcast[4];
+    int ibcast[4];
+};
+
+// Exclusive prefix sum over the CTA (thread order) of a 64-bit value; returns
+// the prefix and writes the total to *total.
+__device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v, SmpShared &sm,
+                                                              unsigned long long *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) sm.wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        unsigned long long t = sm.wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        sm.wsum[lane] = t;  // inclusive over warps
+    }
+    __syncthreads();
+    const unsigned long long before = (w > 0 ? sm.wsum[w - 1] : 0ull);
+    *total = sm.wsum[31];
+    return before + x - v;
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, SmpShared &sm) {
+    unsigned long long tot;
+    block_excl_scan(v, sm, &tot);
+    return tot;
+}
+
+// Over the 4096 (+1 top) buckets of sm.hist: the largest bucket index h with
+// base + sum_{h' >= h} hist[h'] >= target (-1 if none); *above receives
+// base + sum_{h' > h} hist[h'].  nb = number of buckets (4097 or 4096).
+__device__ __forceinline__ int find_cut(SmpShared &sm, int nb, unsigned long long base,
+                                        unsigned long long target, unsigned long long *above) {
+    // thread t owns buckets [4t, 4t + 4); bucket 4096 (if nb == 4097) is added to base.
+    const int t = threadIdx.x;
+    unsigned long long top = (nb == NBUCKET) ? sm.hist[4096] : 0ull;
+    unsigned long long mine = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mine += sm.hist[4 * t + j];
+    // suffix sum: total - inclusive prefix
+    unsigned long long total;
+    const unsigned long long excl = block_excl_scan(mine, sm, &total);
+    const unsigned long long after_me = total - excl - mine;  // buckets owned by later threads
+    if (t == 0) {
+        sm.ibcast[0] = -1;
+        sm.bcast[0] = 0ull;
+    }
+    __syncthreads();
+    if (nb == NBUCKET && base + top >= target) {
+        if (t == 0) {
+            sm.ibcast[0] = 4096;
+            sm.bcast[0] = base;
+        }
+    } else {
+        unsigned long long run = base + top + after_me;
+        for (int j = 3; j >= 0; --j) {
+            const int h = 4 * t + j;
+            const unsigned long long above_h = run;
+            run += sm.hist[h];
+            if (run >= target && above_h < target) {
+                sm.ibcast[0] = h;  // unique: the suffix sum crosses target exactly once
+                sm.bcast[0] = above_h;
+            }
+        }
+    }
+    __syncthreads();
+    *above = sm.bcast[0];
+    const int h = sm.ibcast[0];
+    __syncthreads();
+    return h;
+}
+
+// Same with counts instead of sums (hist holds counts).
+__global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SmpShared &sm = *reinterpret_cast<SmpShared *>(smem_raw);
+    const int b = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_launch();
+    const int slot = p.slots[b];
+    if (slot < 0 || slot >= p.n_slots) {
+        if (tid == 0) {
+            atomicOr(p.err, ERR_SLOT);
+            p.next[b] = 0;
+        }
+        return;
+    }
+    const SampleParamsDev sp = p.params[slot];
+    const int V = p.V;
+    const float *lg = p.logits + (size_t)b * V;
+
+    if (sp.greedy || !(sp.temperature > 0.0f)) {
+        float best = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int i = tid; i < V; i += SMP_THREADS) {
+            const float v = lg[i];
+            if (v > best || (v == best && i < bi)) {
+                best = v;
+                bi = i;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > best || (ov == best && oi < bi)) {
+                best = ov;
+                bi = oi;
+            }
+        }
+        if ((tid & 31) == 0) {
+            sm.wf[tid >> 5] = best;
+            sm.wi[tid >> 5] = bi;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float bv = sm.wf[0];
+            int bj = sm.wi[0];
+            for (int w = 1; w < 32; ++w)
+                if (sm.wf[w] > bv || (sm.wf[w] == bv && sm.wi[w] < bj)) {
+                    bv = sm.wf[w];
+                    bj = sm.wi[w];
+                }
+            p.next[b] = (bj < V) ? bj : 0;
+        }
+        return;
+    }
+
+    float *occ = p.occ + (size_t)slot * V;
+    float *lp = p.lpen + (size_t)b * V;
+    // ---- pass A: penalty and max
+    float mx = -INFINITY;
+    for (int i = tid; i < V; i += SMP_THREADS) {
+        const float o = occ[i];
+        const float pres = o > 0.0f ? sp.presence : 0.0f;
+        float t = __fmul_rn(o, sp.frequency);
+        t = __fadd_rn(pres, t);
+        const float l = __fsub_rn(lg[i], t);
+        lp[i] = l;
+        mx = fmaxf(mx, l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((tid & 31) == 0) sm.wf[tid >> 5] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float m = sm.wf[0];
+        for (int w = 1; w < 32; ++w) m = fmaxf(m, sm.wf[w]);
+        sm.wf[0] = m;
+    }
+    __syncthreads();
+    const float m = sm.wf[0];
+    __syncthreads();
+
+    // ---- pass B: weight sums per (q1 >> 12) bucket
+    for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+    __syncthreads();
+    unsigned long long q1loc = 0;
+    for (int i = tid; i < V; i += SMP_THREADS) {
+        const uint32_t q = qweight(lp[i], m, 1.0f);
+        q1loc += q;
+        if (q) atomicAdd(&sm.hist[q >> 12], (unsigned long long)q);
+    }
+    const unsigned long long Q1 = block_sum_u64(q1loc, sm);
+    unsigned long long target = (unsigned long long)ceil(__dmul_rn((double)sp.top_p, (double)Q1));
+    if (target < 1ull) target = 1ull;
+    if (target > Q1) target = Q1;
+    unsigned long long above;
+    const int hb = find_cut(sm, NBUCKET, 0ull, target, &above);
+    // ---- pass C: low 12 bits within bucket hb
+    for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+    __syncthreads();
+    for (int i = tid; i < V; i += SMP_THREADS) {
+        const uint32_t q = qweight(lp[i], m, 1.0f);
+        if ((int)(q >> 12) == hb && q) atomicAdd(&sm.hist[q & 4095u], (unsigned long long)q);
+    }
+    __syncthreads();
+    unsigned long long above2;
+    const int lo = find_cut(sm, 4096, above, target, &above2);
+    const uint32_t tp = ((uint32_t)hb << 12) | (uint32_t)(lo < 0 ? 0 : lo);
+
+    // ---- optional top-k: t_k = k-th largest q1 (counts), ties by lowest index
+    const bool use_k = sp.top_k > 0 && sp.top_k < V;
+    uint32_t tk = 0;
+    unsigned long long need_ties = 0;
+    if (use_k) {
+        const unsigned long long K = (unsigned long long)sp.top_k;
+        for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+        __syncthreads();
+        for (int i = tid; i < V; i += SMP_THREADS) atomicAdd(&sm.hist[qweight(lp[i], m, 1.0f) >> 12], 1ull);
+        __syncthreads();
+        unsigned long long cabove;
+        const int hk = find_cut(sm, NBUCKET, 0ull, K, &cabove);
+        for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+        __syncthreads();
+        for (int i = tid; i < V; i += SMP_THREADS) {
+            const uint32_t q = qweight(lp[i], m, 1.0f);
+            if ((int)(q >> 12) == hk) atomicAdd(&sm.hist[q & 4095u], 1ull);
+        }
+        __syncthreads();
+        unsigned long long cgt;
+        const int lk = find_cut(sm, 4096, cabove, K, &cgt);
+        tk = ((uint32_t)hk << 12) | (uint32_t)(lk < 0 ? 0 : lk);
+        need_ties = K - cgt;  // elements equal to tk to keep (lowest indices first)
+    }
+
+    // ---- pass D: kept set, qT, exclusive scan in index order, draw, pick
+    const int C = (V + SMP_THREADS - 1) / SMP_THREADS;
+    const int i_lo = tid * C, i_hi = min(V, i_lo + C);
+    unsigned long long tie_base = 0;
+    if (use_k) {
+        unsigned long long ties = 0;
+        for (int i = i_lo; i < i_hi; ++i) ties += (qweight(lp[i], m, 1.0f) == tk);
+        unsigned long long tt;
+        tie_base = block_excl_scan(ties, sm, &tt);
+    }
+    unsigned long long rloc = 0;
+    {
+        unsigned long long tie_seen = tie_base;
+        for (int i = i_lo; i < i_hi; ++i) {
+            const uint32_t q = qweight(lp[i], m, 1.0f);
+            bool keep = q >= tp;
+            if (use_k) {
+                const bool tie = (q == tk);
+                keep = keep && (q > tk || (tie && tie_seen < need_ties));
+                tie_seen += tie;
+            }
+            if (keep) rloc += (sp.temperature == 1.0f) ? q : qweight(lp[i], m, sp.temperature);
+        }
+    }
+    unsigned long long R;
+    const unsigned long long rbase = block_excl_scan(rloc, sm, &R);
+    const unsigned long long nd = p.ndraw[slot];
+    uint32_t ctr[4] = {(uint32_t)nd, (uint32_t)(nd >> 32), 0u, 0u};
+    philox4x32_10(ctr, (uint32_t)sp.seed, (uint32_t)(sp.seed >> 32));
+    const unsigned long long u = (unsigned long long)ctr[0] | ((unsigned long long)ctr[1] << 32);
+    const unsigned long long r = __umul64hi(u, R);
+    if (tid == 0) sm.ibcast[1] = -1;
+    __syncthreads();
+    if (rloc > 0 && rbase <= r && r < rbase + rloc) {
+        unsigned long long acc = rbase, tie_seen = tie_base;
+        for (int i = i_lo; i < i_hi; ++i) {
+            const uint32_t q = qweight(lp[i], m, 1.0f);
+            bool keep = q >= tp;
+            if (use_k) {
+                const bool tie = (q == tk);
+                keep = keep && (q > tk || (tie && tie_seen < need_ties));
+                tie_seen += tie;
+            }
+            if (!keep) continue;
+            acc += (sp.temperature == 1.0f) ? q : qweight(lp[i], m, sp.temperature);
+            if (acc > r) {
+                sm.ibcast[1] = i;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    const int tok = sm.ibcast[1];
+    // ---- pass E: occurrence decay and count
+    if (tok >= 0) {
+        for (int i = tid; i < V; i += SMP_THREADS) occ[i] = __fmul_rn(occ[i], sp.penalty_decay);
+        __syncthreads();
+        if (tid == 0) occ[tok] = __fadd_rn(occ[tok], 1.0f);
+    }
+    if (tid == 0) {
+        p.next[b] = tok >= 0 ? tok : 0;
+        if (tok < 0) atomicOr(p.err, ERR_CONFIG);
+        p.ndraw[slot] = nd + 1ull;
+    }
+}
+
+void launch_sampler(const SamplerParams &p, const LaunchCfg &lc, cudaError_t *e) {
+    static bool attr_set = false;
+    const size_t smem = sizeof(SmpShared);
+    if (!attr_set) {
+        cudaError_t r = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (r != cudaSuccess) {
+            *e = r;
+            return;
+        }
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B);
+    cfg.blockDim = dim3(SMP_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = lc.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = lc.pdl ? 1 : 0;
+    cudaError_t r = cudaLaunchKernelEx(&cfg, sampler_kernel, p);
+    if (r != cudaSuccess) *e = r;
+}
+
+}  // namespace rk

@@ -1,0 +1,56 @@
+"""Shared helpers of the GPU parity tests: build a library context and an oracle
+model on the same seeded weights, and compare their outputs.
+
+Acceptance (fp16 weights, fp32 state): logits max-abs <= 2e-2 and cosine
+>= 0.9999 against the oracle; greedy tokens identical wherever the oracle's
+top-1/top-2 margin exceeds the logit tolerance (below it both picks are correct
+readings of the same logits); sampled tokens bit-exact given identical logits."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+LOGIT_ATOL = 2e-2
+LOGIT_COS = 0.9999
+
+
+def gpu_ctx(shape: str, n_slots: int, weights: dict | None = None, mode: int = 0):
+    import recurrent_decode_gb300 as rd
+    dims = synth.Dims(shape)
+    if weights is None:
+        weights = synth.make_weights(shape)
+    ctx = rd.Rwkv7(dims, n_slots)
+    ctx.set_weights(weights)
+    ctx.set_mode(mode)
+    return ctx, weights, dims
+
+
+def cosine(a, b):
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
+
+
+def assert_logits_close(gpu, ref, what=""):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.max(np.abs(gpu - ref))
+    cos = cosine(gpu, ref)
+    assert err <= LOGIT_ATOL and cos >= LOGIT_COS, f"{what}: max|d|={err:.3e} cos={cos:.7f}"
+    return err, cos
+
+
+def greedy_consistent(gpu_token: int, ref_logits) -> bool:
+    """The GPU's greedy token is the oracle's argmax, or within the tolerance of it."""
+    ref = np.asarray(ref_logits, np.float64)
+    best = int(np.argmax(ref))
+    if gpu_token == best:
+        return True
+    return ref[best] - ref[gpu_token] <= 2 * LOGIT_ATOL
+
+
+def oracle_states(weights, dims, n):
+    m = oracle.Model(weights, dims)
+    return m, [m.new_state() for _ in range(n)]
