@@ -10,10 +10,58 @@
 
 namespace rk {
 
-constexpr int LN_THREADS = 256;
-constexpr int LN_MAXV = 32;  // d <= 8192
+// LayerNorm kernels: one CTA per slot row, 8 consecutive elements per thread
+// (16-byte loads), blockDim = d/8 rounded up to a warp.
+__device__ __forceinline__ void h8_to_f(const uint4 &u, float (&f)[8]) {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 t = __half22float2(h[k]);
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+    }
+}
+__device__ __forceinline__ uint4 f_to_h8(const float (&f)[8]) {
+    uint4 u;
+    __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+    return u;
+}
+__device__ __forceinline__ void ld8f(const float *p, float (&f)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void st8f(float *p, const float (&f)[8]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+}
 
-// Sum over the CTA (blockDim = LN_THREADS).  `red` holds 32 floats.
+// x[8] += sum over j < nsplit of part[j * stride + off .. +8], slabs added in
+// order j = 0, 1, ... (loads issued four slabs at a time).
+__device__ __forceinline__ void add_slabs(float (&x)[8], const float *part, int nsplit, long long stride, size_t off) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int j = 0;
+    for (; j + 4 <= nsplit; j += 4) {
+        float t[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ld8f(part + (size_t)(j + u) * stride + off, t[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] += t[u][k];
+    }
+    for (; j < nsplit; ++j) {
+        float t[8];
+        ld8f(part + (size_t)j * stride + off, t);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] += t[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] += acc[k];
+}
+
+// Sum over the CTA.  `red` holds 32 floats.
 __device__ __forceinline__ float block_sum(float v, float *red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_sum(v);
@@ -25,41 +73,41 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return t;
 }
 
-// LayerNorm of the values v[j] = x[tid + j*blockDim] (j < cnt, d values in all),
-// in place: (x - mean) / sqrt(var + eps) * w + b with biased variance.
-__device__ __forceinline__ void block_layernorm(float (&v)[LN_MAXV], int d, const __half *w, const __half *b,
-                                                float *red) {
-    const int cnt = (d + LN_THREADS - 1) / LN_THREADS;
+// In-place LayerNorm of the d values held 8 per thread (inactive threads hold
+// zeros): (x - mean) / sqrt(var + 1e-5) * w + b, biased variance.
+__device__ __forceinline__ void ln8(float (&v)[8], bool act, int d, const uint4 &w4, const uint4 &b4, float *red) {
     float s = 0.0f;
 #pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j)
-        if (j < cnt && threadIdx.x + j * LN_THREADS < d) s += v[j];
+    for (int k = 0; k < 8; ++k) s += v[k];
     const float mean = block_sum(s, red) / (float)d;
     float q = 0.0f;
+    if (act) {
 #pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j)
-        if (j < cnt && threadIdx.x + j * LN_THREADS < d) {
-            float t = v[j] - mean;
+        for (int k = 0; k < 8; ++k) {
+            const float t = v[k] - mean;
             q += t * t;
         }
+    }
     const float var = block_sum(q, red) / (float)d;
     const float rs = 1.0f / sqrtf(var + 1e-5f);
+    float w[8], b[8];
+    h8_to_f(w4, w);
+    h8_to_f(b4, b);
 #pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j) {
-        const int i = threadIdx.x + j * LN_THREADS;
-        if (j < cnt && i < d) v[j] = (v[j] - mean) * rs * __half2float(w[i]) + __half2float(b[i]);
-    }
+    for (int k = 0; k < 8; ++k) v[k] = (v[k] - mean) * rs * w[k] + b[k];
 }
 
 // x[b] = LN0(emb[token[b]]).  Also validates the step's slots and tokens:
 // range errors are latched and the row falls back to token 0; CTA 0 looks for
 // repeated slots with a bitmap in shared memory.
-__global__ void __launch_bounds__(LN_THREADS) embed_kernel(const ElemParams p) {
+__global__ void embed_kernel(const ElemParams p) {
     extern __shared__ uint32_t bitmap[];
     __shared__ float red[32];
     pdl_wait();
     pdl_launch();
     const int b = blockIdx.x;
+    const int i0 = threadIdx.x * 8;
+    const bool act = i0 < p.d;
     const int slot = p.slots[b];
     int tok = p.tokens[b];
     if (threadIdx.x == 0) {
@@ -67,21 +115,15 @@ __global__ void __launch_bounds__(LN_THREADS) embed_kernel(const ElemParams p) {
         if (tok < 0 || tok >= p.V) atomicOr(p.err, ERR_TOKEN);
     }
     if (tok < 0 || tok >= p.V) tok = 0;
-    const __half *e = p.emb + (size_t)tok * p.d;
-    float v[LN_MAXV];
-    const int cnt = (p.d + LN_THREADS - 1) / LN_THREADS;
-#pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j) {
-        const int i = threadIdx.x + j * LN_THREADS;
-        v[j] = (j < cnt && i < p.d) ? __half2float(e[i]) : 0.0f;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint4 w4 = make_uint4(0, 0, 0, 0), b4 = w4;
+    if (act) {
+        h8_to_f(*reinterpret_cast<const uint4 *>(p.emb + (size_t)tok * p.d + i0), v);
+        w4 = *reinterpret_cast<const uint4 *>(p.ln_w + i0);
+        b4 = *reinterpret_cast<const uint4 *>(p.ln_b + i0);
     }
-    block_layernorm(v, p.d, p.ln_w, p.ln_b, red);
-    float *xr = p.x + (size_t)b * p.d;
-#pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j) {
-        const int i = threadIdx.x + j * LN_THREADS;
-        if (j < cnt && i < p.d) xr[i] = v[j];
-    }
+    ln8(v, act, p.d, w4, b4, red);
+    if (act) st8f(p.x + (size_t)b * p.d + i0, v);
     if (b == 0) {
         const int words = (p.n_slots + 31) / 32;
         for (int i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
@@ -97,59 +139,73 @@ __global__ void __launch_bounds__(LN_THREADS) embed_kernel(const ElemParams p) {
 }
 
 // xl = LN(x[b]); for each mix q: xo[q][b] = fp16(xl + (shift - xl) * mu_q); shift <- xl.
-// nmix = 6 for the time mix (r, w, k, v, a, g), 1 for the channel mix.
-__global__ void __launch_bounds__(LN_THREADS) ln_mix_kernel(const ElemParams p, int nmix) {
+// NMIX = 6 for the time mix (r, w, k, v, a, g), 1 for the channel mix.  The
+// constants and the shift state (written only by this kernel, one step
+// earlier) are fetched before the dependency wait.
+template <int NMIX>
+__global__ void ln_mix_kernel(const ElemParams p) {
     __shared__ float red[32];
     const int b = blockIdx.x;
+    const int i0 = threadIdx.x * 8;
+    const bool act = i0 < p.d;
     const int slot = p.slots[b];
     const bool ok = slot >= 0 && slot < p.n_slots;
+    uint4 w4 = make_uint4(0, 0, 0, 0), b4 = w4, mu4[NMIX];
+    float sh[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float *shp = p.shift + (size_t)(ok ? slot : 0) * p.d + i0;
+    if (act) {
+        w4 = *reinterpret_cast<const uint4 *>(p.ln_w + i0);
+        b4 = *reinterpret_cast<const uint4 *>(p.ln_b + i0);
+#pragma unroll
+        for (int q = 0; q < NMIX; ++q) mu4[q] = *reinterpret_cast<const uint4 *>(p.mu[q] + i0);
+        if (ok) ld8f(shp, sh);
+    }
     pdl_wait();
     pdl_launch();
-    const float *xr = p.x + (size_t)b * p.d;
-    float v[LN_MAXV];
-    const int cnt = (p.d + LN_THREADS - 1) / LN_THREADS;
-#pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j) {
-        const int i = threadIdx.x + j * LN_THREADS;
-        v[j] = (j < cnt && i < p.d) ? xr[i] : 0.0f;
-    }
-    block_layernorm(v, p.d, p.ln_w, p.ln_b, red);
-    float *sh = p.shift + (size_t)(ok ? slot : 0) * p.d;
-#pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j) {
-        const int i = threadIdx.x + j * LN_THREADS;
-        if (j < cnt && i < p.d) {
-            const float xl = v[j];
-            const float prev = ok ? sh[i] : 0.0f;
-            const float dlt = prev - xl;
-            for (int q = 0; q < nmix; ++q)
-                p.xo[q][(size_t)b * p.d + i] = __float2half_rn(xl + dlt * __half2float(p.mu[q][i]));
-            if (ok) sh[i] = xl;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (act) {
+        ld8f(p.x + (size_t)b * p.d + i0, v);
+        if (p.part) {
+            add_slabs(v, p.part, p.nsplit, p.split_stride, (size_t)b * p.d + i0);
+            st8f(p.x + (size_t)b * p.d + i0, v);
         }
     }
+    ln8(v, act, p.d, w4, b4, red);
+    if (!act) return;
+#pragma unroll
+    for (int q = 0; q < NMIX; ++q) {
+        float mu[8], o[8];
+        h8_to_f(mu4[q], mu);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = v[k] + (sh[k] - v[k]) * mu[k];
+        *reinterpret_cast<uint4 *>(p.xo[q] + (size_t)b * p.d + i0) = f_to_h8(o);
+    }
+    if (ok) st8f(shp, v);
 }
 
 // xo[0][b] = fp16(LN_out(x[b])): the input of the head projection.
-__global__ void __launch_bounds__(LN_THREADS) ln_out_kernel(const ElemParams p) {
+__global__ void ln_out_kernel(const ElemParams p) {
     __shared__ float red[32];
     const int b = blockIdx.x;
+    const int i0 = threadIdx.x * 8;
+    const bool act = i0 < p.d;
+    uint4 w4 = make_uint4(0, 0, 0, 0), b4 = w4;
+    if (act) {
+        w4 = *reinterpret_cast<const uint4 *>(p.ln_w + i0);
+        b4 = *reinterpret_cast<const uint4 *>(p.ln_b + i0);
+    }
     pdl_wait();
     pdl_launch();
-    const float *xr = p.x + (size_t)b * p.d;
-    float v[LN_MAXV];
-    const int cnt = (p.d + LN_THREADS - 1) / LN_THREADS;
-#pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j) {
-        const int i = threadIdx.x + j * LN_THREADS;
-        v[j] = (j < cnt && i < p.d) ? xr[i] : 0.0f;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (act) {
+        ld8f(p.x + (size_t)b * p.d + i0, v);
+        if (p.part) add_slabs(v, p.part, p.nsplit, p.split_stride, (size_t)b * p.d + i0);
     }
-    block_layernorm(v, p.d, p.ln_w, p.ln_b, red);
-#pragma unroll
-    for (int j = 0; j < LN_MAXV; ++j) {
-        const int i = threadIdx.x + j * LN_THREADS;
-        if (j < cnt && i < p.d) p.xo[0][(size_t)b * p.d + i] = __float2half_rn(v[j]);
-    }
+    ln8(v, act, p.d, w4, b4, red);
+    if (act) *reinterpret_cast<uint4 *>(p.xo[0] + (size_t)b * p.d + i0) = f_to_h8(v);
 }
+
+static int ln_threads(int d) { return ((d / 8) + 31) / 32 * 32; }
 
 // ---------------------------------------------------------------------------
 // WKV7: one CTA per (head h, slot row b), 256 threads.  Thread t holds state
@@ -191,9 +247,14 @@ __global__ void __launch_bounds__(256) wkv_kernel(const WkvParams p) {
     float kk = 0.f, kv = 0.f, av = 0.f, vv = 0.f;
     if (tid < HS) {
         const int c = h * HS + tid;
-        kv = p.k[off + tid];
+        float rv = 0.f;
+        for (int j = 0; j < p.nsplit; ++j) {  // add the projection's k-split slabs in order
+            const size_t o = (size_t)j * p.split_stride + off + tid;
+            rv += p.r[o];
+            kv += p.k[o];
+            vv += p.v[o];
+        }
         av = p.a[off + tid];
-        vv = p.v[off + tid];
         kk = kv * __half2float(p.k_k[c]);
         const float ss = sum64(kk * kk, s_red, 1);
         const float nrm = fmaxf(sqrtf(ss), 1e-12f);
@@ -212,7 +273,7 @@ __global__ void __launch_bounds__(256) wkv_kernel(const WkvParams p) {
         s_dec[tid] = p.dec[off + tid];
         s_kp[tid] = kpv;
         s_vp[tid] = vpv;
-        s_r[tid] = p.r[off + tid];
+        s_r[tid] = rv;
     }
     __syncthreads();
     const float4 kh = *(const float4 *)&s_kh[cg * 4];
@@ -253,6 +314,28 @@ __global__ void __launch_bounds__(256) wkv_kernel(const WkvParams p) {
         const float bonus = sum64(s_r[tid] * s_kp[tid] * __half2float(p.r_k[c]), s_red, 1);
         const float zv = (yn + bonus * s_vp[tid]) * p.g[off + tid];
         p.z[off + tid] = __float2half_rn(zv);
+    }
+}
+
+// LoRA-down outputs: one CTA per slot row; column c of LoRA i is the sum of the
+// S partial slabs, passed through the LoRA's activation and rounded to fp16.
+__global__ void lora_fin_kernel(const LoraFinParams p) {
+    const int b = blockIdx.x;
+    pdl_wait();
+    pdl_launch();
+    const int total = p.r[0] + p.r[1] + p.r[2] + p.r[3];
+    for (int c = threadIdx.x; c < total; c += blockDim.x) {
+        int i = 0, col = c;
+        while (col >= p.r[i]) {
+            col -= p.r[i];
+            ++i;
+        }
+        const float *src = p.part[i] + (size_t)b * p.r[i] + col;
+        const long long stride = (long long)p.bcap * p.r[i];
+        float acc = 0.0f;
+        for (int j = 0; j < p.S; ++j) acc += src[(size_t)j * stride];
+        const float y = p.act[i] == 1 ? tanhf(acc) : (p.act[i] == 2 ? 1.0f / (1.0f + expf(-acc)) : acc);
+        p.out[i][(size_t)b * p.r[i] + col] = __float2half_rn(y);
     }
 }
 
@@ -330,21 +413,21 @@ static cudaLaunchConfig_t mkcfg(dim3 grid, dim3 block, size_t smem, const Launch
 void launch_embed(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e) {
     cudaLaunchAttribute at[1];
     const size_t smem = (size_t)((p.n_slots + 31) / 32) * 4;
-    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(LN_THREADS), smem, lc, at);
+    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(ln_threads(p.d)), smem, lc, at);
     cudaError_t r = cudaLaunchKernelEx(&cfg, embed_kernel, p);
     if (r != cudaSuccess) *e = r;
 }
 
 void launch_ln_mix(const ElemParams &p, int nmix, const LaunchCfg &lc, cudaError_t *e) {
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(LN_THREADS), 0, lc, at);
-    cudaError_t r = cudaLaunchKernelEx(&cfg, ln_mix_kernel, p, nmix);
+    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(ln_threads(p.d)), 0, lc, at);
+    cudaError_t r = nmix == 6 ? cudaLaunchKernelEx(&cfg, ln_mix_kernel<6>, p) : cudaLaunchKernelEx(&cfg, ln_mix_kernel<1>, p);
     if (r != cudaSuccess) *e = r;
 }
 
 void launch_ln_out(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e) {
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(LN_THREADS), 0, lc, at);
+    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(ln_threads(p.d)), 0, lc, at);
     cudaError_t r = cudaLaunchKernelEx(&cfg, ln_out_kernel, p);
     if (r != cudaSuccess) *e = r;
 }
@@ -353,6 +436,13 @@ void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e) {
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = mkcfg(dim3(p.H, p.B), dim3(256), 0, lc, at);
     cudaError_t r = cudaLaunchKernelEx(&cfg, wkv_kernel, p);
+    if (r != cudaSuccess) *e = r;
+}
+
+void launch_lora_fin(const LoraFinParams &p, const LaunchCfg &lc, cudaError_t *e) {
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(256), 0, lc, at);
+    cudaError_t r = cudaLaunchKernelEx(&cfg, lora_fin_kernel, p);
     if (r != cudaSuccess) *e = r;
 }
 

@@ -9,35 +9,39 @@
 // to 16), so one pass over the weights serves the whole batch.
 //
 //  * tensor-core kernel: one CTA per SM, warp-specialised -- warp 0 issues TMA
-//    loads of 128x64 weight tiles and Bx64 activation tiles into a ring of
-//    shared-memory stages, warp 1 issues tcgen05.mma into a TMEM accumulator,
-//    warps 2-5 drain TMEM and apply the epilogue.  The (tile, k-block) units of
-//    all segments are split evenly over the grid (stream-K); a tile whose
-//    k-range spans several CTAs is reduced by the last CTA to arrive, summing
-//    the partials in CTA order so the result does not depend on timing.
-//  * SIMT kernel: a plain warp-per-row dot product with the same epilogues,
-//    kept as an independent cross-check of the tensor-core kernel.
+//    loads of 16 KB weight tiles (stored contiguously, so each load is one
+//    sequential 16 KB read) and Bx64 activation tiles into a ring of
+//    shared-memory stages, warp 1 issues tcgen05.mma into a TMEM accumulator
+//    (two buffers when they fit, so the next item's MMAs overlap the previous
+//    epilogue), warps 2-5 drain TMEM and apply the epilogue.  Work items are
+//    (row tile, k-range) pairs split evenly over the grid; a split k-range
+//    stores fp32 partial sums that the consuming kernel adds in a fixed order,
+//    so no CTA waits for another and results do not depend on timing.
+//  * SIMT kernel: a plain warp-per-row dot product with the same epilogues and
+//    partial layout, kept as an independent cross-check of the tensor-core kernel.
 #include "internal.cuh"
 
 namespace rk {
 
+constexpr uint32_t W_TILE_BYTES = GEMM_TILE_M * GEMM_TILE_K * 2;  // 16 KB
+// A pipeline stage holds KB_STAGE consecutive k-blocks: one TMA copy of the
+// adjacent weight tiles (32 KB) and one activation box per k-block.
+constexpr int KB_STAGE = 2;
+constexpr uint32_t W_STAGE_BYTES = KB_STAGE * W_TILE_BYTES;
+
 __device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
 
-// Apply the segment's epilogue to one result.  Returns the fp16 value stored
-// for EPI_RELU2 (so the caller can record sparsity), else 0.
-__device__ __forceinline__ bool epi_store(const GemmSeg &s, int n, int b, float acc) {
+// Apply the segment's epilogue to one result.  Returns true when EPI_RELU2
+// stores a nonzero fp16 value (so the caller can record sparsity).
+__device__ __forceinline__ bool epi_store(const GemmSeg &s, int n, int b, float acc, float bias) {
     size_t o = (size_t)b * s.ldo + n;
     switch (s.epi) {
         case EPI_F32: ((float *)s.out)[o] = acc; break;
         case EPI_F16: ((__half *)s.out)[o] = __float2half_rn(acc); break;
         case EPI_F16_TANH: ((__half *)s.out)[o] = __float2half_rn(tanhf(acc)); break;
         case EPI_F16_SIGMOID: ((__half *)s.out)[o] = __float2half_rn(sigm(acc)); break;
-        case EPI_DECAY: {
-            float t = __half2float(s.bias[n]) + acc;
-            ((float *)s.out)[o] = expf(-0.606530659712633f * sigm(t));
-            break;
-        }
-        case EPI_SIGMOID_BIAS: ((float *)s.out)[o] = sigm(__half2float(s.bias[n]) + acc); break;
+        case EPI_DECAY: ((float *)s.out)[o] = expf(-0.606530659712633f * sigm(bias + acc)); break;
+        case EPI_SIGMOID_BIAS: ((float *)s.out)[o] = sigm(bias + acc); break;
         case EPI_RESID: ((float *)s.out)[o] += acc; break;
         case EPI_RELU2: {
             float t = fmaxf(acc, 0.0f);
@@ -50,70 +54,133 @@ __device__ __forceinline__ bool epi_store(const GemmSeg &s, int n, int b, float 
     return false;
 }
 
-// ---------------------------------------------------------------------------
-// Work partition: units (tile, k-block) numbered tile-major; CTA c owns
-// [start(c), start(c+1)).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int unit_start(int c, int G, int U) { return (int)(((long long)c * U) / G); }
-__device__ __forceinline__ int cta_of_unit(int u, int G, int U) {
-    return (int)((((long long)(u + 1)) * G + U - 1) / U) - 1;
+// Epilogue of 16 consecutive slot rows b0..b0+15 of weight row n for split j:
+// the segment's epilogue when it is not split, else the raw fp32 partial.
+__device__ __forceinline__ bool epi_chunk(const GemmSeg &s, int n, int j, int b0, const float (&v)[16], int B) {
+    if (n >= s.rows) return false;
+    if (s.S > 1) {
+        float *out = (float *)s.out + (size_t)j * s.split_stride;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (b0 + q < B) out[(size_t)(b0 + q) * s.ldo + n] = v[q];
+        return false;
+    }
+    if (s.epi == EPI_RESID) {
+        float *out = (float *)s.out;
+        float old[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) old[q] = (b0 + q < B) ? out[(size_t)(b0 + q) * s.ldo + n] : 0.0f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (b0 + q < B) out[(size_t)(b0 + q) * s.ldo + n] = old[q] + v[q];
+        return false;
+    }
+    const float bias = (s.bias != nullptr) ? __half2float(s.bias[n]) : 0.0f;
+    bool nz = false;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        if (b0 + q < B) nz |= epi_store(s, n, b0 + q, v[q], bias);
+    return nz;
 }
 
-struct Loc {
-    int s, tin, kblk, tile;  // segment, tile within segment, k-block, global tile
+// ---------------------------------------------------------------------------
+// Work partition: global items numbered segment by segment, item = (row tile,
+// split); CTA c owns items [first(c), first(c+1)).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int item_first(int c, int G, int I) { return (int)(((long long)c * I) / G); }
+
+struct Item {
+    int s, tile, split, kb0, kb1;
 };
-__device__ __forceinline__ Loc locate(const GemmParams &p, int u) {
+__device__ __forceinline__ Item locate_item(const GemmSeg *seg, int nseg, int i) {
     int s = 0;
-    while (s + 1 < p.nseg && u >= p.seg[s + 1].unit0) ++s;
-    int r = u - p.seg[s].unit0;
-    int kb = p.seg[s].kb;
-    Loc l;
-    l.s = s;
-    l.tin = r / kb;
-    l.kblk = r - l.tin * kb;
-    l.tile = p.seg[s].tile0 + l.tin;
-    return l;
+    while (s + 1 < nseg && i >= seg[s + 1].item0) ++s;
+    const GemmSeg &g = seg[s];
+    const int local = i - g.item0;
+    Item it;
+    it.s = s;
+    it.tile = local / g.S;
+    it.split = local - it.tile * g.S;
+    const int np = g.kb / KB_STAGE;  // k-block pairs of the segment
+    it.kb0 = (int)(((long long)it.split * np) / g.S) * KB_STAGE;
+    it.kb1 = (int)(((long long)(it.split + 1) * np) / g.S) * KB_STAGE;
+    return it;
 }
-__device__ __forceinline__ bool unit_skipped(const GemmParams &p, int kblk) {
-    return p.nz_skip != nullptr && p.nz_skip[kblk] == 0u;
+// Flags of all-zero activation k-blocks, staged in shared memory (nullptr: none
+// skipped).  A stage (k-blocks kb, kb+1) is skipped when both are all zero.
+__device__ __forceinline__ bool kblock_skipped(const uint32_t *flags, int kblk) {
+    return flags != nullptr && flags[kblk] == 0u;
 }
+__device__ __forceinline__ bool stage_skipped(const uint32_t *flags, int kb) {
+    return flags != nullptr && flags[kb] == 0u && flags[kb + 1] == 0u;
+}
+constexpr int MAX_NZ_BLOCKS = 1024;  // d_ffn / 64
 
-constexpr uint32_t W_TILE_BYTES = GEMM_TILE_M * GEMM_TILE_K * 2;  // 16 KB
 
 __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
+    // Segment descriptors and sparsity flags are staged in shared memory and the
+    // scalars in registers: the parameter block is only addressed for the tensor
+    // maps, so nothing in the loops re-reads it.
+    __shared__ GemmSeg sseg[GEMM_MAX_SEG];
+    __shared__ uint32_t snz[MAX_NZ_BLOCKS];
+    __shared__ uint64_t flags_ready;
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int S = p.stages;
-    const uint32_t XB = (uint32_t)p.npad * 128u;
+    const int S = p.stages, B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, nitems = p.nitems;
+    const bool has_skip = p.nz_skip != nullptr;
+    const uint32_t *skip = has_skip ? snz : nullptr;
+    const uint32_t XKB = (uint32_t)npad * 128u;  // one activation k-block
+    const uint32_t XB = KB_STAGE * XKB;            // per stage
     uint8_t *sW = base;
-    uint8_t *sX = base + (size_t)S * W_TILE_BYTES;
+    uint8_t *sX = base + (size_t)S * W_STAGE_BYTES;
     uint64_t *full = (uint64_t *)(sX + (size_t)S * XB);
     uint64_t *empty = full + S;
-    uint64_t *acc_full = empty + S;
-    uint64_t *acc_empty = acc_full + 1;
-    uint32_t *tmem_slot = (uint32_t *)(acc_empty + 1);
+    uint64_t *acc_full = empty + S;      // [2]
+    uint64_t *acc_empty = acc_full + 2;  // [2]
+    uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    volatile uint32_t *ticket_s = tmem_slot + 2;
     volatile uint32_t *nzq = tmem_slot + 3;  // [4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = gridDim.x, c = blockIdx.x, U = p.nunits;
-    const int u_begin = unit_start(c, G, U), u_end = unit_start(c + 1, G, U);
+    const int G = gridDim.x, c = blockIdx.x;
+    const int i_begin = item_first(c, G, nitems), i_end = item_first(c + 1, G, nitems);
     uint32_t ncols = 32;
-    while ((int)ncols < p.npad) ncols <<= 1;
+    while ((int)ncols < NB * npad) ncols <<= 1;
 
+    if (threadIdx.x < nseg) sseg[threadIdx.x] = p.seg[threadIdx.x];
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 128);
+        }
+        mbar_init(&flags_ready, 1);
         *abort_flag = 0u;
         fence_barrier_init();
     }
+    __syncthreads();
+
+    // Weight prefetch before the dependency wait (weights are constant), issued
+    // before the TMEM allocation so it proceeds even while a predecessor's CTA
+    // still holds tensor memory on this SM.
+    int npre = 0;
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.maps[i]);
+        if (p.prefetch) {
+            const uint64_t polW = policy_evict_first();
+            for (int i = i_begin; i < i_end && npre < S; ++i) {
+                const Item it = locate_item(sseg, nseg, i);
+                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
+                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
+                for (int kb = it.kb0; kb < it.kb1 && npre < S; kb += KB_STAGE, ++npre) {
+                    mbar_expect_tx(&full[npre], W_STAGE_BYTES + XB);
+                    tma_load_3d(sW + (size_t)npre * W_STAGE_BYTES, wm, &full[npre], 0, 0, tb + kb, polW);
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, ncols);
@@ -128,94 +195,82 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t polW = policy_evict_first(), polX = policy_evict_last();
-            int npre = 0;
-            if (p.prefetch) {
-                for (int u = u_begin; u < u_end && npre < S; ++u, ++npre) {
-                    Loc l = locate(p, u);
-                    const GemmSeg &sg = p.seg[l.s];
-                    mbar_expect_tx(&full[npre], W_TILE_BYTES + XB);
-                    tma_load_3d(sW + (size_t)npre * W_TILE_BYTES, &p.maps[sg.wmap], &full[npre],
-                                l.kblk * GEMM_TILE_K, l.tin * GEMM_TILE_M, sg.layer, polW);
-                }
-            }
             pdl_wait();
             pdl_launch();
-            for (int j = 0; j < npre; ++j) {
-                Loc l = locate(p, u_begin + j);
-                const GemmSeg &sg = p.seg[l.s];
-                for (int r = 0; r < p.npad; r += 16)
-                    tma_load_2d(sX + (size_t)j * XB + (size_t)r * 128, &p.maps[sg.xmap], &full[j],
-                                l.kblk * GEMM_TILE_K, r, polX);
-            }
-            int i = npre;
-            for (int u = u_begin + npre; u < u_end; ++u) {
-                Loc l = locate(p, u);
-                if (unit_skipped(p, l.kblk)) continue;
-                const GemmSeg &sg = p.seg[l.s];
-                const int st = i % S;
-                if (i >= S && !mbar_wait(&empty[st], (uint32_t)((i / S) - 1) & 1u, abort_flag)) {
-                    *abort_flag = 1u;
-                    atomicOr(p.err, ERR_TIMEOUT);
-                    break;
+            bool ok = true;
+            if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
+            int q = 0;  // stage sequence number
+            for (int i = i_begin; i < i_end && ok; ++i) {
+                const Item it = locate_item(sseg, nseg, i);
+                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
+                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
+                const CUtensorMap *xm = &p.maps[sseg[it.s].xmap];
+                for (int kb = it.kb0; kb < it.kb1; kb += KB_STAGE) {
+                    if (stage_skipped(skip, kb)) continue;
+                    const int st = q % S;
+                    if (q >= npre) {
+                        if (q >= S && !mbar_wait(&empty[st], (uint32_t)((q / S) - 1) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(&full[st], W_STAGE_BYTES + XB);
+                        tma_load_3d(sW + (size_t)st * W_STAGE_BYTES, wm, &full[st], 0, 0, tb + kb, polW);
+                    }  // else: the weights were requested before the dependency wait
+#pragma unroll
+                    for (int h = 0; h < KB_STAGE; ++h)
+                        tma_load_2d(sX + (size_t)st * XB + (size_t)h * XKB, xm, &full[st], (kb + h) * GEMM_TILE_K, 0,
+                                    polX);
+                    ++q;
                 }
-                mbar_expect_tx(&full[st], W_TILE_BYTES + XB);
-                tma_load_3d(sW + (size_t)st * W_TILE_BYTES, &p.maps[sg.wmap], &full[st], l.kblk * GEMM_TILE_K,
-                            l.tin * GEMM_TILE_M, sg.layer, polW);
-                for (int r = 0; r < p.npad; r += 16)
-                    tma_load_2d(sX + (size_t)st * XB + (size_t)r * 128, &p.maps[sg.xmap], &full[st],
-                                l.kblk * GEMM_TILE_K, r, polX);
-                ++i;
             }
-            // Before leaving, make sure no copy issued by this CTA is still in flight
-            // (bounded: the last S stages).
-            for (int j = (i > S ? i - S : 0); j < i; ++j) {
+            if (!ok) {
+                *abort_flag = 1u;
+                atomicOr(p.err, ERR_TIMEOUT);
+            }
+            // Before leaving, wait (bounded) until no copy issued here is in flight.
+            for (int j = (q > S ? q - S : 0); j < q; ++j)
                 if (!mbar_wait(&full[j % S], (uint32_t)(j / S) & 1u, abort_flag)) break;
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            pdl_wait();
-            const uint32_t idesc = idesc_f16(GEMM_TILE_M, p.npad);
-            int i = 0, range = 0;
-            int u = u_begin;
+            const uint32_t idesc = idesc_f16(GEMM_TILE_M, npad);
             bool ok = true;
-            while (u < u_end && ok) {
-                Loc l = locate(p, u);
-                const GemmSeg &sg = p.seg[l.s];
-                int r_end = sg.unit0 + (l.tin + 1) * sg.kb;
-                if (r_end > u_end) r_end = u_end;
-                if (range > 0 && !mbar_wait(acc_empty, (uint32_t)(range - 1) & 1u, abort_flag)) {
+            if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
+            int q = 0, n = 0;
+            for (int i = i_begin; i < i_end && ok; ++i, ++n) {
+                const Item it = locate_item(sseg, nseg, i);
+                const int buf = n % NB;
+                if (n >= NB && !mbar_wait(&acc_empty[buf], (uint32_t)((n / NB) - 1) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * npad);
                 uint32_t issued = 0;
-                for (; u < r_end; ++u) {
-                    int kblk = locate(p, u).kblk;
-                    if (unit_skipped(p, kblk)) continue;
-                    const int st = i % S;
-                    if (!mbar_wait(&full[st], (uint32_t)(i / S) & 1u, abort_flag)) {
+                for (int kb = it.kb0; kb < it.kb1; kb += KB_STAGE) {
+                    if (stage_skipped(skip, kb)) continue;
+                    const int st = q % S;
+                    if (!mbar_wait(&full[st], (uint32_t)(q / S) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sW + (size_t)st * W_TILE_BYTES);
+                    const uint32_t a0 = smem_u32(sW + (size_t)st * W_STAGE_BYTES);
                     const uint32_t b0 = smem_u32(sX + (size_t)st * XB);
 #pragma unroll
-                    for (int kk = 0; kk < GEMM_TILE_K / 16; ++kk)
-                        mma_f16(tmem, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32), idesc,
-                                (issued | (uint32_t)kk) ? 1u : 0u);
+                    for (int kk = 0; kk < KB_STAGE * GEMM_TILE_K / 16; ++kk)
+                        mma_f16(d_tmem, sdesc_k128(a0 + (kk >> 2) * W_TILE_BYTES + (kk & 3) * 32),
+                                sdesc_k128(b0 + (kk >> 2) * XKB + (kk & 3) * 32), idesc, (issued | (uint32_t)kk) ? 1u : 0u);
                     issued = 1;
                     mma_commit(&empty[st]);
-                    ++i;
+                    ++q;
                 }
                 if (!ok) break;
                 if (issued)
-                    mma_commit(acc_full);
+                    mma_commit(&acc_full[buf]);
                 else
-                    mbar_arrive(acc_full);
-                ++range;
+                    mbar_arrive(&acc_full[buf]);
             }
             if (!ok) {
                 *abort_flag = 1u;
@@ -225,106 +280,58 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         pdl_wait();
-        const int q = warp & 3;               // TMEM lane quarter of this warp
-        const int row = q * 32 + lane;        // accumulator row = weight row within the tile
+        const int qd = warp & 3;              // TMEM lane quarter of this warp
+        const int row = qd * 32 + lane;       // accumulator row = weight row within the tile
         const int et = threadIdx.x - 64;      // 0..127
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-        int range = 0;
-        int u = u_begin;
-        while (u < u_end) {
-            Loc l = locate(p, u);
-            const GemmSeg &sg = p.seg[l.s];
-            const int tile_u0 = sg.unit0 + l.tin * sg.kb;
-            int r_end = tile_u0 + sg.kb;
-            const bool complete = (u == tile_u0) && (r_end <= u_end);
-            if (r_end > u_end) r_end = u_end;
+        uint32_t *nz_out = p.nz_out;
+        if (has_skip) {  // stage the k-block flags written by the preceding kernel
+            const int nkb = sseg[0].kb < MAX_NZ_BLOCKS ? sseg[0].kb : MAX_NZ_BLOCKS;  // padded count
+            const int nreal = (sseg[0].K + GEMM_TILE_K - 1) / GEMM_TILE_K;             // flags written
+            for (int j = et; j < nkb; j += 128) snz[j] = j < nreal ? p.nz_skip[j] : 0u;
+            named_bar(1, 128);
+            if (et == 0) mbar_arrive(&flags_ready);
+        }
+        int n = 0;
+        for (int i = i_begin; i < i_end; ++i, ++n) {
+            const Item it = locate_item(sseg, nseg, i);
+            const GemmSeg sg = sseg[it.s];  // register copy
+            const int buf = n % NB;
             bool valid = false;
-            for (int uu = u; uu < r_end; ++uu)
-                if (!unit_skipped(p, uu - tile_u0)) valid = true;
-            if (!mbar_wait(acc_full, (uint32_t)range & 1u, abort_flag)) {
+            for (int kb = it.kb0; kb < it.kb1; kb += KB_STAGE)
+                if (!stage_skipped(skip, kb)) valid = true;
+            if (!mbar_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u, abort_flag)) {
                 *abort_flag = 1u;
                 atomicOr(p.err, ERR_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            const int n = l.tin * GEMM_TILE_M + row;
+            const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
+            const int nrow = it.tile * GEMM_TILE_M + row;
             bool nzany = false;
-            if (complete) {
-                for (int cb = 0; cb < p.npad; cb += 16) {
-                    float v[16];
-                    if (valid) {
-                        tmem_ld16(taddr + (uint32_t)cb, v);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int b = cb + j;
-                        if (b < p.B && n < sg.rows) nzany |= epi_store(sg, n, b, v[j]);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(acc_empty);
-            } else {
-                const int first_tile = locate(p, u_begin).tile;
-                const int myslot = (l.tile == first_tile) ? 0 : 1;
-                float *wsp = p.ws + ((size_t)(c * 2 + myslot) * p.npad) * GEMM_TILE_M;
-                for (int cb = 0; cb < p.npad; cb += 16) {
-                    float v[16];
-                    if (valid) {
-                        tmem_ld16(taddr + (uint32_t)cb, v);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int b = cb + j;
-                        if (b < p.B) __stcg(&wsp[(size_t)b * GEMM_TILE_M + row], v[j]);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(acc_empty);
-                __threadfence();
-                named_bar(1, 128);
-                if (et == 0) *ticket_s = atomicAdd(&p.counters[l.tile], 1u);
-                named_bar(1, 128);
-                const int c_first = cta_of_unit(tile_u0, G, U);
-                const int c_last = cta_of_unit(tile_u0 + sg.kb - 1, G, U);
-                const uint32_t ncontrib = (uint32_t)(c_last - c_first + 1);
-                if (*ticket_s == ncontrib - 1u) {
-                    __threadfence();
-                    for (int b = 0; b < p.B; ++b) {
-                        float acc = 0.0f;
-                        for (int cc = c_first; cc <= c_last; ++cc) {
-                            const int ft = locate(p, unit_start(cc, G, U)).tile;
-                            const int sl = (ft == l.tile) ? 0 : 1;
-                            acc += __ldcg(&p.ws[((size_t)(cc * 2 + sl) * p.npad + b) * GEMM_TILE_M + row]);
-                        }
-                        if (n < sg.rows) nzany |= epi_store(sg, n, b, acc);
-                    }
-                    if (et == 0) p.counters[l.tile] = 0u;
+            for (int cb = 0; cb < npad; cb += 16) {
+                float v[16];
+                if (valid) {
+                    tmem_ld16(taddr + (uint32_t)cb, v);
                 } else {
-                    ++range;
-                    u = r_end;
-                    continue;  // another CTA finalises this tile
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = 0.0f;
                 }
+                nzany |= epi_chunk(sg, nrow, it.split, cb, v, B);
             }
-            if (sg.epi == EPI_RELU2 && p.nz_out != nullptr) {
+            tc_fence_before();
+            mbar_arrive(&acc_empty[buf]);
+            if (sg.epi == EPI_RELU2 && sg.S == 1 && nz_out != nullptr) {
                 const unsigned bal = __ballot_sync(0xffffffffu, nzany);
-                if (lane == 0) nzq[q] = bal ? 1u : 0u;
+                if (lane == 0) nzq[qd] = bal ? 1u : 0u;
                 named_bar(2, 128);
                 if (et == 0) {
-                    const int blk0 = l.tin * 2;
+                    const int blk0 = it.tile * 2;
                     const int nblk = (sg.rows + 63) / 64;
-                    if (blk0 < nblk) p.nz_out[blk0] = nzq[0] | nzq[1];
-                    if (blk0 + 1 < nblk) p.nz_out[blk0 + 1] = nzq[2] | nzq[3];
+                    if (blk0 < nblk) nz_out[blk0] = nzq[0] | nzq[1];
+                    if (blk0 + 1 < nblk) nz_out[blk0 + 1] = nzq[2] | nzq[3];
                 }
                 named_bar(2, 128);
             }
-            ++range;
-            u = r_end;
         }
     }
 
@@ -337,10 +344,12 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 }
 
 size_t gemm_tc_smem_bytes(int npad, int stages) {
-    return 1024 + (size_t)stages * (W_TILE_BYTES + (size_t)npad * 128) + (size_t)(2 * stages + 2) * 8 + 64;
+    return 1024 + (size_t)stages * (W_STAGE_BYTES + (size_t)KB_STAGE * npad * 128) + (size_t)(2 * stages + 4) * 8 + 64;
 }
 
-int gemm_tc_max_smem() { return 227 * 1024; }
+size_t gemm_tc_stage_bytes(int npad) { return W_STAGE_BYTES + (size_t)KB_STAGE * npad * 128; }
+
+int gemm_tc_max_smem() { return 220 * 1024; }  // dynamic part; static staging takes ~5 KB
 
 void launch_gemm_tc(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e) {
     static bool attr_set = false;
@@ -368,15 +377,18 @@ void launch_gemm_tc(const GemmParams &p, int grid, size_t smem, const LaunchCfg 
 }
 
 // ---------------------------------------------------------------------------
-// SIMT cross-check kernel: CTA = 64 output rows of one segment, warp = 8 rows.
-// seg.tile0 holds the segment's first 64-row block.
+// SIMT cross-check kernel: CTA = 64 output rows x one split of one segment,
+// warp = 8 rows; reads the tiled weight layout directly.  seg.item0 holds the
+// segment's first CTA (64-row block x split).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ GemmParams p) {
     __shared__ uint32_t nzw[8];
     int s = 0;
-    while (s + 1 < p.nseg && (int)blockIdx.x >= p.seg[s + 1].tile0) ++s;
+    while (s + 1 < p.nseg && (int)blockIdx.x >= p.seg[s + 1].item0) ++s;
     const GemmSeg &sg = p.seg[s];
-    const int blk = blockIdx.x - sg.tile0;
+    const int local = blockIdx.x - sg.item0;
+    const int blk = local / sg.S, split = local % sg.S;
+    const int kb0 = (int)(((long long)split * sg.kb) / sg.S), kb1 = (int)(((long long)(split + 1) * sg.kb) / sg.S);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_launch();
@@ -384,14 +396,16 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
     for (int rr = 0; rr < 8; ++rr) {
         const int n = blk * 64 + warp * 8 + rr;
         if (n >= sg.rows) break;
-        const __half *wrow = sg.w + (size_t)n * sg.K;
+        const int tr = n / GEMM_TILE_M, rin = n % GEMM_TILE_M;
         for (int b0 = 0; b0 < p.B; b0 += 8) {
             float acc[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-            for (int k = lane * 8; k < sg.K; k += 256) {
-                if (unit_skipped(p, k / GEMM_TILE_K)) continue;
-                const uint4 wv = *(const uint4 *)(wrow + k);
+            for (int k = kb0 * GEMM_TILE_K + lane * 8; k < kb1 * GEMM_TILE_K && k < sg.K; k += 256) {
+                if (kblock_skipped(p.nz_skip, k / GEMM_TILE_K)) continue;
+                const __half *wp = sg.w + (((size_t)tr * sg.kb + k / GEMM_TILE_K) * GEMM_TILE_M + rin) * GEMM_TILE_K +
+                                   (k % GEMM_TILE_K);
+                const uint4 wv = *(const uint4 *)wp;
                 const __half2 *w2 = (const __half2 *)&wv;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -414,11 +428,19 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 #pragma unroll
                 for (int j = 1; j < 8; ++j)
                     if (lane == j) v = acc[j];
-                nzany |= epi_store(sg, n, b0 + lane, v);
+                const int b = b0 + lane;
+                if (sg.S > 1) {
+                    ((float *)sg.out)[(size_t)split * sg.split_stride + (size_t)b * sg.ldo + n] = v;
+                } else if (sg.epi == EPI_RESID) {
+                    ((float *)sg.out)[(size_t)b * sg.ldo + n] += v;
+                } else {
+                    const float bias = (sg.bias != nullptr) ? __half2float(sg.bias[n]) : 0.0f;
+                    nzany |= epi_store(sg, n, b, v, bias);
+                }
             }
         }
     }
-    if (sg.epi == EPI_RELU2 && p.nz_out != nullptr) {
+    if (sg.epi == EPI_RELU2 && sg.S == 1 && p.nz_out != nullptr) {
         const unsigned bal = __ballot_sync(0xffffffffu, nzany);
         if (lane == 0) nzw[warp] = bal ? 1u : 0u;
         __syncthreads();
@@ -432,7 +454,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 
 void launch_gemm_simt(const GemmParams &p, const LaunchCfg &lc, cudaError_t *e) {
     int nblk = 0;
-    for (int s = 0; s < p.nseg; ++s) nblk += (p.seg[s].rows + 63) / 64;
+    for (int s = 0; s < p.nseg; ++s) nblk += ((p.seg[s].rows + 63) / 64) * p.seg[s].S;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nblk);
     cfg.blockDim = dim3(256);

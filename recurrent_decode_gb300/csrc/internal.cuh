@@ -26,6 +26,7 @@ constexpr int GEMM_TILE_M = 128;   // weight rows per tile (MMA M)
 constexpr int GEMM_TILE_K = 64;    // reduction elements per stage (128 bytes of fp16)
 constexpr int GEMM_MAX_SEG = 8;
 constexpr int GEMM_MAX_MAPS = 16;
+constexpr int MAX_SPLIT = 16;         // k-splits of one projection
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bounded waits give up after ~2 s
 
 // Epilogue kinds of the projection GEMM.  acc is the fp32 dot product of one
@@ -41,16 +42,24 @@ enum Epi : int {
     EPI_RELU2 = 7,       // out f16 = relu(acc)^2, plus a nonzero flag per 64 rows
 };
 
+// One weight matrix of a projection launch.  Weights are stored tile-major:
+// tile (row block tr, k-block kb) of 128 rows x 64 k fp16 is 16 KB contiguous,
+// tiles ordered (layer, tr, kb); ragged rows / k are zero-padded.  A segment's
+// row tiles are split into S contiguous k-ranges ("items"): S == 1 applies the
+// epilogue, S > 1 stores raw fp32 partial sums, slab j at out + j*split_stride,
+// which the consuming kernel adds in slab order.
 struct GemmSeg {
     int wmap, xmap;       // tensor-map indices (tensor-core path)
-    int layer;            // layer coordinate of the weight map
+    int tile_base;        // map tile index of (this layer, row tile 0, k-block 0)
     int rows, K, kb;      // output rows, reduction length, k-blocks of 64
-    int tile0, unit0;     // first global tile / unit of this segment
+    int tiles, S;         // row tiles, k-splits
+    int item0;            // first global item of this segment
     int epi;
     void *out;
-    int ldo;              // out element index = b * ldo + n
+    int ldo;              // out element index = b * ldo + n (+ j * split_stride)
+    long long split_stride;
     const __half *bias;   // [rows] (EPI_DECAY / EPI_SIGMOID_BIAS)
-    const __half *w;      // row-major weights [rows][K] of this layer (SIMT path)
+    const __half *w;      // tiled weights of this layer (SIMT path)
     const __half *x;      // activations [B][ldx] (SIMT path)
     int ldx;
 };
@@ -58,14 +67,13 @@ struct GemmSeg {
 struct GemmParams {
     CUtensorMap maps[GEMM_MAX_MAPS]; // weight and activation maps used by the segments
     GemmSeg seg[GEMM_MAX_SEG];
-    int nseg, nmaps, ntiles, nunits;
+    int nseg, nmaps, nitems;
     int B, npad;                     // slots in the step, MMA N (B rounded up to 16)
     int stages;                      // smem pipeline depth
+    int accbufs;                     // TMEM accumulator buffers (1 or 2)
     int prefetch;                    // 1: weights may be fetched before the dependency wait
     uint32_t *nz_out;                // EPI_RELU2: flag per 64 output rows
     const uint32_t *nz_skip;         // nonzero flags per k-block of the activations (or null)
-    float *ws;                       // split-K partials [grid][2][npad][128]
-    uint32_t *counters;              // per-tile arrival tickets (left at zero)
     uint32_t *err;
 };
 
@@ -78,6 +86,7 @@ struct LaunchCfg {
 void launch_gemm_tc(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e);
 void launch_gemm_simt(const GemmParams &p, const LaunchCfg &lc, cudaError_t *e);
 size_t gemm_tc_smem_bytes(int npad, int stages);
+size_t gemm_tc_stage_bytes(int npad);
 int gemm_tc_max_smem();
 
 struct ElemParams {
@@ -89,6 +98,9 @@ struct ElemParams {
     const __half *mu[6];      // token-shift mixes
     __half *xo[6];            // mixed outputs [B][d]
     float *shift;             // shift state base of this layer [n_slots][d]
+    const float *part;        // residual partial slabs to add to x first (or null)
+    int nsplit;
+    long long split_stride;
     uint32_t *err;
 };
 
@@ -99,7 +111,10 @@ void launch_ln_out(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
 struct WkvParams {
     int B, d, H, n_slots, layer;
     const int32_t *slots;
-    const float *r, *k, *v, *dec, *a, *vg, *g;  // [B][d]
+    const float *r, *k, *v;                      // partial slabs [nsplit][.][d]
+    int nsplit;
+    long long split_stride;
+    const float *dec, *a, *vg, *g;               // [B][d]
     float *v_first;                              // [B][d]
     const __half *k_k, *k_a, *r_k, *lnx_w, *lnx_b;
     float *wkv;                                  // this layer's states [n_slots][H][64][64]
@@ -107,6 +122,17 @@ struct WkvParams {
     uint32_t *err;
 };
 void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e);
+
+// LoRA-down outputs: add the S partial slabs, apply the activation (0 none,
+// 1 tanh, 2 sigmoid), round to fp16.  r[i] == 0 skips LoRA i.
+struct LoraFinParams {
+    int B, S, bcap;
+    int r[4];
+    int act[4];
+    const float *part[4];  // [S][bcap][r]
+    __half *out[4];        // [B][r]
+};
+void launch_lora_fin(const LoraFinParams &p, const LaunchCfg &lc, cudaError_t *e);
 
 struct SampleParamsDev {  // device copy of one slot's sampling parameters
     float temperature, top_p;

@@ -82,12 +82,15 @@ struct rwkv7_ctx {
     int L = 0, d = 0, H = 0, F = 0, V = 0, rw = 0, ra = 0, rv = 0, rg = 0, n_slots = 0;
     int bcap = 0;  // activation rows (max slots per fused step, rounded up to 16)
     int nsm = 0;
-    cudaStream_t stream = nullptr;
+    cudaStream_t stream = nullptr;      // caller's stream: every call is ordered on it
+    cudaStream_t cap_stream = nullptr;  // private stream used only to capture step graphs
     int mode = 0;
     std::string err;
 
-    // weights
+    // weights: vectors and the embedding row-major; projection matrices tile-major
+    // (tiled[k]: [layer][row tile][k-block][128][64] fp16, zero-padded)
     int wrows[W_COUNT]{}, wcols[W_COUNT]{};
+    bool tiled[W_COUNT]{};
     __half *w[W_COUNT]{};
     std::vector<uint8_t> wset;  // [W_COUNT][L] (globals use index 0)
     size_t n_missing = 0;
@@ -105,14 +108,18 @@ struct rwkv7_ctx {
           *vfirst = nullptr, *x = nullptr, *logits = nullptr, *lpen = nullptr;
     uint32_t *nz = nullptr;
     int32_t *slots = nullptr, *tokens = nullptr, *next = nullptr;
-    float *ws = nullptr;
-    uint32_t *counters = nullptr;
+    // split-K partial sums [MAX_SPLIT][bcap][cols] fp32: r, k, v, the LoRA-down
+    // outputs (w, a, v, g) and the residual-stream contributions
+    float *pr = nullptr, *pk = nullptr, *pv = nullptr, *phw = nullptr, *pha = nullptr, *phv = nullptr,
+          *phg = nullptr, *px = nullptr;
     uint32_t *errw = nullptr;
-    size_t ws_floats = 0;
 
     CUtensorMap wmap[W_COUNT]{};
     bool has_wmap[W_COUNT]{};
-    CUtensorMap amap[A_COUNT]{};
+    CUtensorMap amap[A_COUNT][MAX_B / 16]{};
+    bool amap_ok[A_COUNT][MAX_B / 16]{};
+    void *abase[A_COUNT]{};
+    int acols[A_COUNT]{};
 
     std::map<std::tuple<int, int, int, int>, cudaGraphExec_t> graphs;
     std::vector<void *> allocs;
@@ -153,6 +160,11 @@ int dalloc(rwkv7_ctx *c, T **p, size_t count) {
 
 bool per_layer(int kind) { return kind >= FIRST_LAYER_KIND; }
 
+int env_int(const char *name, int dflt) {
+    const char *v = getenv(name);
+    return (v && *v) ? atoi(v) : dflt;
+}
+
 int make_map(rwkv7_ctx *c, CUtensorMap *m, void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
              const uint32_t *box) {
     auto fn = encode_fn();
@@ -171,22 +183,51 @@ int make_map(rwkv7_ctx *c, CUtensorMap *m, void *base, int rank, const uint64_t 
     return RWKV7_OK;
 }
 
-// Weight map: 3D {cols (K), rows, layers}, box {64, 128, 1}.
+int row_tiles(const rwkv7_ctx *c, int kind) { return (c->wrows[kind] + GEMM_TILE_M - 1) / GEMM_TILE_M; }
+// k-blocks of 64, padded to an even count (the GEMM moves two per pipeline stage)
+int kblocks(const rwkv7_ctx *c, int kind) { return ((c->wcols[kind] + GEMM_TILE_K - 1) / GEMM_TILE_K + 1) & ~1; }
+size_t layer_elems(const rwkv7_ctx *c, int kind) {
+    return c->tiled[kind] ? (size_t)row_tiles(c, kind) * kblocks(c, kind) * GEMM_TILE_M * GEMM_TILE_K
+                          : (size_t)c->wrows[kind] * c->wcols[kind];
+}
+
+// Weight map over the tile-major layout: 3D {64 k, 128 rows, all tiles of all
+// layers}, box {64, 128, 2}: every load is two adjacent k-block tiles, 32 KB
+// contiguous.
 int make_wmap(rwkv7_ctx *c, int kind) {
     const int layers = per_layer(kind) ? c->L : 1;
-    uint64_t dims[3] = {(uint64_t)c->wcols[kind], (uint64_t)c->wrows[kind], (uint64_t)layers};
-    uint64_t strides[2] = {(uint64_t)c->wcols[kind] * 2, (uint64_t)c->wcols[kind] * c->wrows[kind] * 2};
-    uint32_t box[3] = {64, 128, 1};
+    const uint64_t ntiles = (uint64_t)layers * row_tiles(c, kind) * kblocks(c, kind);
+    uint64_t dims[3] = {(uint64_t)GEMM_TILE_K, (uint64_t)GEMM_TILE_M, ntiles};
+    uint64_t strides[2] = {(uint64_t)GEMM_TILE_K * 2, (uint64_t)GEMM_TILE_K * GEMM_TILE_M * 2};
+    uint32_t box[3] = {64, 128, 2};
     c->has_wmap[kind] = true;
     return make_map(c, &c->wmap[kind], c->w[kind], 3, dims, strides, box);
 }
 
-// Activation map: 2D {cols (K), bcap rows}, box {64, 16}.
+// Split factor of a launch whose segments hold `tiles` row tiles in all:
+// enough k-splits that every SM gets about one item.
+int split_for(const rwkv7_ctx *c, int tiles) {
+    int s = c->nsm / std::max(1, tiles);
+    return std::max(1, std::min(s, MAX_SPLIT));
+}
+
+// Activation map: 2D {cols (K), bcap rows}, box {64, npad}: one copy per
+// k-block brings every slot row of the step.  Encoded lazily per npad.
 int make_amap(rwkv7_ctx *c, int which, void *base, int cols) {
-    uint64_t dims[2] = {(uint64_t)cols, (uint64_t)c->bcap};
-    uint64_t strides[1] = {(uint64_t)cols * 2};
-    uint32_t box[2] = {64, 16};
-    return make_map(c, &c->amap[which], base, 2, dims, strides, box);
+    c->abase[which] = base;
+    c->acols[which] = cols;
+    return RWKV7_OK;
+}
+const CUtensorMap *get_amap(rwkv7_ctx *c, int which, int npad) {
+    CUtensorMap &m = c->amap[which][npad / 16 - 1];
+    if (!c->amap_ok[which][npad / 16 - 1]) {
+        uint64_t dims[2] = {(uint64_t)c->acols[which], (uint64_t)c->bcap};
+        uint64_t strides[1] = {(uint64_t)c->acols[which] * 2};
+        uint32_t box[2] = {64, (uint32_t)npad};
+        if (make_map(c, &m, c->abase[which], 2, dims, strides, box) != RWKV7_OK) return nullptr;
+        c->amap_ok[which][npad / 16 - 1] = true;
+    }
+    return &m;
 }
 
 // ---------------------------------------------------------------- GEMM launches
@@ -199,6 +240,7 @@ struct Seg {
     void *out;
     int ldo;
     const __half *bias;
+    int S;        // k-splits (S > 1: raw fp32 partials, slab stride bcap * ldo)
 };
 
 int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *nz_out, const uint32_t *nz_skip,
@@ -209,11 +251,13 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
     int wslot[W_COUNT], aslot[A_COUNT];
     for (int i = 0; i < W_COUNT; ++i) wslot[i] = -1;
     for (int i = 0; i < A_COUNT; ++i) aslot[i] = -1;
-    int tile = 0, unit = 0, blk = 0;
+    int item = 0, blk = 0;
     for (int s = 0; s < n; ++s) {
         const Seg &sg = segs[s];
         GemmSeg &g = p.seg[s];
         const int rows = c->wrows[sg.wkind];
+        if (!c->tiled[sg.wkind] || sg.K != c->wcols[sg.wkind] || sg.S < 1 || sg.S > MAX_SPLIT)
+            return fail(c, RWKV7_ECUDA, "internal: bad GEMM segment");
         if (wslot[sg.wkind] < 0) {
             if (nmaps >= GEMM_MAX_MAPS) return fail(c, RWKV7_ECUDA, "too many tensor maps in one GEMM");
             wslot[sg.wkind] = nmaps;
@@ -221,76 +265,72 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         }
         if (aslot[sg.xbuf] < 0) {
             if (nmaps >= GEMM_MAX_MAPS) return fail(c, RWKV7_ECUDA, "too many tensor maps in one GEMM");
+            const CUtensorMap *am = get_amap(c, sg.xbuf, (B + 15) / 16 * 16);
+            if (!am) return RWKV7_ECUDA;
             aslot[sg.xbuf] = nmaps;
-            p.maps[nmaps++] = c->amap[sg.xbuf];
+            p.maps[nmaps++] = *am;
         }
         g.wmap = wslot[sg.wkind];
         g.xmap = aslot[sg.xbuf];
-        g.layer = per_layer(sg.wkind) ? layer : 0;
         g.rows = rows;
         g.K = sg.K;
-        g.kb = (sg.K + GEMM_TILE_K - 1) / GEMM_TILE_K;
+        g.kb = kblocks(c, sg.wkind);
+        g.tiles = row_tiles(c, sg.wkind);
+        g.S = std::min(sg.S, g.kb / 2);
+        g.tile_base = (per_layer(sg.wkind) ? layer : 0) * g.tiles * g.kb;
         g.epi = sg.epi;
         g.out = sg.out;
         g.ldo = sg.ldo;
+        g.split_stride = (long long)c->bcap * sg.ldo;
         g.bias = sg.bias;
-        g.w = c->w[sg.wkind] + (size_t)g.layer * rows * sg.K;
+        g.w = c->w[sg.wkind] + (size_t)(per_layer(sg.wkind) ? layer : 0) * layer_elems(c, sg.wkind);
         g.x = sg.xptr;
         g.ldx = sg.K;
         if (mode == 2) {
-            g.tile0 = blk;
-            blk += (rows + 63) / 64;
+            g.item0 = blk;
+            blk += ((rows + 63) / 64) * g.S;
         } else {
-            g.tile0 = tile;
-            g.unit0 = unit;
-            const int tiles = (rows + GEMM_TILE_M - 1) / GEMM_TILE_M;
-            tile += tiles;
-            unit += tiles * g.kb;
+            g.item0 = item;
+            item += g.tiles * g.S;
         }
     }
     p.nseg = n;
     p.nmaps = nmaps;
-    p.ntiles = tile;
-    p.nunits = unit;
+    p.nitems = item;
     p.B = B;
     p.npad = (B + 15) / 16 * 16;
     p.nz_out = nz_out;
     p.nz_skip = nz_skip;
-    p.ws = c->ws;
-    p.counters = c->counters;
     p.err = c->errw;
     cudaError_t e = cudaSuccess;
     if (mode == 2) {
         launch_gemm_simt(p, lc, &e);
     } else {
-        // one CTA per SM; a small pipeline leaves room for the next kernel's CTA
-        const size_t stage = 16384 + (size_t)p.npad * 128;
-        int stages;
-        if (p.npad <= 64)
-            stages = (int)std::min<size_t>(6, (112 * 1024 - 2048) / stage);
-        else
-            stages = (int)std::min<size_t>(8, (220 * 1024 - 2048) / stage);
-        if (stages < 2) stages = 2;
+        // CTAs per SM and pipeline depth: by default one CTA per SM with the
+        // deepest pipeline that fits; RWKV7_GEMM_CTAS_PER_SM / RWKV7_GEMM_STAGES
+        // override them (tuning knobs).
+        const size_t stage = gemm_tc_stage_bytes(p.npad);
+        const int per_sm = std::max(1, std::min(4, env_int("RWKV7_GEMM_CTAS_PER_SM", 1)));
+        const size_t budget = (size_t)gemm_tc_max_smem() / per_sm - (per_sm > 1 ? 8192 : 2048);
+        int stages = (int)std::min<size_t>(6, budget / stage);
+        stages = std::max(2, std::min(stages, env_int("RWKV7_GEMM_STAGES", stages)));
         p.stages = stages;
+        p.accbufs = (2 * p.npad * per_sm <= 256) ? 2 : 1;
         p.prefetch = nz_skip == nullptr ? 1 : 0;
-        int grid = std::min(p.nunits, c->nsm);
-        if ((size_t)grid * 2 * p.npad * GEMM_TILE_M > c->ws_floats) return fail(c, RWKV7_ECUDA, "workspace too small");
-        if (p.ntiles > 4096) return fail(c, RWKV7_ECUDA, "too many tiles");
+        const int grid = std::min(p.nitems, c->nsm * per_sm);
         launch_gemm_tc(p, grid, gemm_tc_smem_bytes(p.npad, stages), lc, &e);
     }
     if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return RWKV7_OK;
 }
 
-const __half *LW(rwkv7_ctx *c, int kind, int l) {
-    return c->w[kind] + (size_t)l * c->wrows[kind] * c->wcols[kind];
-}
+const __half *LW(rwkv7_ctx *c, int kind, int l) { return c->w[kind] + (size_t)l * layer_elems(c, kind); }
 
 // Enqueue one fused step for rows [0, B) of the activation buffers (slots and
 // tokens already in c->slots / c->tokens).
-int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf = nullptr) {
-    LaunchCfg lc{c->stream, mode != 2 && pf == nullptr};
-    LaunchCfg lc0{c->stream, false};
+int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, int mode, Prof *pf = nullptr) {
+    LaunchCfg lc{st, mode != 2 && pf == nullptr};
+    LaunchCfg lc0{st, false};
     cudaError_t e = cudaSuccess;
     // optional CUDA-event bracketing of every launch (profiling mode only)
     auto pb = [&](int cls) {
@@ -303,10 +343,10 @@ int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf
             }
         }
         pf->cls.push_back(cls);
-        cudaEventRecord(pf->ev[pf->n++], c->stream);
+        cudaEventRecord(pf->ev[pf->n++], st);
     };
     auto pe = [&]() {
-        if (pf) cudaEventRecord(pf->ev[pf->n++], c->stream);
+        if (pf) cudaEventRecord(pf->ev[pf->n++], st);
     };
     const int d = c->d;
     ElemParams ep;
@@ -330,8 +370,16 @@ int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf
     pe();
     if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "embed launch: %s", cudaGetErrorString(e));
     int rc;
+    // Split factors depend only on the shapes, so a slot's result does not depend on B.
+    const int s1 = std::min(split_for(c, 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) +
+                                             row_tiles(c, L_V1) + row_tiles(c, L_G1)),
+                            kblocks(c, L_WR) / 2);
+    const int s3 = std::min(split_for(c, row_tiles(c, L_WO)), kblocks(c, L_WO) / 2);
+    const int s5 = std::min(split_for(c, row_tiles(c, L_FV)), kblocks(c, L_FV) / 2);
+    const long long xstride = (long long)c->bcap * d;
+    int px_splits = 0;  // residual partial slabs in c->px still to be added to x
     for (int l = 0; l < c->L; ++l) {
-        // LN1 + token shift + 6 mixes
+        // (x += pending partials) + LN1 + token shift + 6 mixes
         ElemParams m = ep;
         m.layer = l;
         m.ln_w = LW(c, L_LN1W, l);
@@ -342,34 +390,51 @@ int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf
             m.xo[q] = c->xmix[q];
         }
         m.shift = c->shift_att + (size_t)l * c->n_slots * d;
+        m.part = px_splits ? c->px : nullptr;
+        m.nsplit = px_splits;
+        m.split_stride = xstride;
         pb(P_LN_MIX);
         launch_ln_mix(m, 6, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
-        // G1: r, k, v and the LoRA down projections
+        // G1: r, k, v and the LoRA down projections, as s1 partial slabs
         Seg g1[7];
         int n1 = 0;
-        g1[n1++] = {L_WR, A_XR, c->xmix[0], d, EPI_F32, c->r, d, nullptr};
-        g1[n1++] = {L_WK, A_XK, c->xmix[2], d, EPI_F32, c->k, d, nullptr};
-        g1[n1++] = {L_WV, A_XV, c->xmix[3], d, EPI_F32, c->v, d, nullptr};
-        g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F16_TANH, c->hw, c->rw, nullptr};
-        g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F16, c->ha, c->ra, nullptr};
-        if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F16, c->hv, c->rv, nullptr};
-        g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F16_SIGMOID, c->hg, c->rg, nullptr};
+        g1[n1++] = {L_WR, A_XR, c->xmix[0], d, EPI_F32, c->pr, d, nullptr, s1};
+        g1[n1++] = {L_WK, A_XK, c->xmix[2], d, EPI_F32, c->pk, d, nullptr, s1};
+        g1[n1++] = {L_WV, A_XV, c->xmix[3], d, EPI_F32, c->pv, d, nullptr, s1};
+        g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F32, c->phw, c->rw, nullptr, s1};
+        g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F32, c->pha, c->ra, nullptr, s1};
+        if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F32, c->phv, c->rv, nullptr, s1};
+        g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, s1};
         pb(P_GEMM_PROJ);
         if ((rc = run_gemm(c, l, g1, n1, B, nullptr, nullptr, lc, mode))) return rc;
         pe();
+        // LoRA down: add the slabs, activation, fp16 (the LoRA-up GEMM's operands)
+        LoraFinParams lf;
+        memset(&lf, 0, sizeof lf);
+        lf.B = B;
+        lf.S = s1;
+        lf.r[0] = c->rw; lf.r[1] = c->ra; lf.r[2] = l > 0 ? c->rv : 0; lf.r[3] = c->rg;
+        lf.part[0] = c->phw; lf.part[1] = c->pha; lf.part[2] = c->phv; lf.part[3] = c->phg;
+        lf.out[0] = c->hw; lf.out[1] = c->ha; lf.out[2] = c->hv; lf.out[3] = c->hg;
+        lf.act[0] = 1; lf.act[1] = 0; lf.act[2] = 0; lf.act[3] = 2;
+        lf.bcap = c->bcap;
+        pb(P_GEMM_LORA);
+        launch_lora_fin(lf, lc, &e);
+        pe();
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "lora_fin launch: %s", cudaGetErrorString(e));
         // G2: LoRA up projections with their gates
         Seg g2[4];
         int n2 = 0;
-        g2[n2++] = {L_W2, A_HW, c->hw, c->rw, EPI_DECAY, c->dec, d, LW(c, L_W0, l)};
-        g2[n2++] = {L_A2, A_HA, c->ha, c->ra, EPI_SIGMOID_BIAS, c->a, d, LW(c, L_A0, l)};
-        if (l > 0) g2[n2++] = {L_V2, A_HV, c->hv, c->rv, EPI_SIGMOID_BIAS, c->vg, d, LW(c, L_V0, l)};
-        g2[n2++] = {L_G2, A_HG, c->hg, c->rg, EPI_F32, c->g, d, nullptr};
+        g2[n2++] = {L_W2, A_HW, c->hw, c->rw, EPI_DECAY, c->dec, d, LW(c, L_W0, l), 1};
+        g2[n2++] = {L_A2, A_HA, c->ha, c->ra, EPI_SIGMOID_BIAS, c->a, d, LW(c, L_A0, l), 1};
+        if (l > 0) g2[n2++] = {L_V2, A_HV, c->hv, c->rv, EPI_SIGMOID_BIAS, c->vg, d, LW(c, L_V0, l), 1};
+        g2[n2++] = {L_G2, A_HG, c->hg, c->rg, EPI_F32, c->g, d, nullptr, 1};
         pb(P_GEMM_LORA);
         if ((rc = run_gemm(c, l, g2, n2, B, nullptr, nullptr, lc, mode))) return rc;
         pe();
-        // WKV7 + GroupNorm + bonus + gate
+        // WKV7 + GroupNorm + bonus + gate (adds the r, k, v slabs)
         WkvParams wp;
         memset(&wp, 0, sizeof wp);
         wp.B = B;
@@ -378,9 +443,11 @@ int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf
         wp.n_slots = c->n_slots;
         wp.layer = l;
         wp.slots = c->slots;
-        wp.r = c->r;
-        wp.k = c->k;
-        wp.v = c->v;
+        wp.r = c->pr;
+        wp.k = c->pk;
+        wp.v = c->pv;
+        wp.nsplit = s1;
+        wp.split_stride = xstride;
         wp.dec = c->dec;
         wp.a = c->a;
         wp.vg = c->vg;
@@ -398,12 +465,13 @@ int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf
         launch_wkv(wp, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "wkv launch: %s", cudaGetErrorString(e));
-        // G3: output projection into the residual
-        Seg g3[1] = {{L_WO, A_Z, c->z, d, EPI_RESID, c->x, d, nullptr}};
+        // G3: output projection, as residual partial slabs
+        Seg g3[1] = {{L_WO, A_Z, c->z, d, EPI_F32, c->px, d, nullptr, s3}};
         pb(P_GEMM_OUT);
         if ((rc = run_gemm(c, l, g3, 1, B, nullptr, nullptr, lc, mode))) return rc;
         pe();
-        // LN2 + token shift + mix
+        px_splits = s3;
+        // (x += slabs) + LN2 + token shift + mix
         ElemParams m2 = ep;
         m2.layer = l;
         m2.ln_w = LW(c, L_LN2W, l);
@@ -411,31 +479,38 @@ int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf
         m2.mu[0] = LW(c, L_FXK, l);
         m2.xo[0] = c->xk;
         m2.shift = c->shift_ffn + (size_t)l * c->n_slots * d;
+        m2.part = c->px;
+        m2.nsplit = px_splits;
+        m2.split_stride = xstride;
         pb(P_LN_MIX);
         launch_ln_mix(m2, 1, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
         // G4: key + ReLU^2 (+ nonzero flags per 64 hidden units)
-        Seg g4[1] = {{L_FK, A_XKF, c->xk, d, EPI_RELU2, c->h, c->F, nullptr}};
+        Seg g4[1] = {{L_FK, A_XKF, c->xk, d, EPI_RELU2, c->h, c->F, nullptr, 1}};
         pb(P_GEMM_KEY);
         if ((rc = run_gemm(c, l, g4, 1, B, c->nz, nullptr, lc, mode))) return rc;
         pe();
-        // G5: value over the nonzero hidden blocks, into the residual
-        Seg g5[1] = {{L_FV, A_H, c->h, c->F, EPI_RESID, c->x, d, nullptr}};
+        // G5: value over the nonzero hidden blocks, as residual partial slabs
+        Seg g5[1] = {{L_FV, A_H, c->h, c->F, EPI_F32, c->px, d, nullptr, s5}};
         pb(P_GEMM_VALUE);
         if ((rc = run_gemm(c, l, g5, 1, B, nullptr, c->nz, lc, mode))) return rc;
         pe();
+        px_splits = s5;
     }
     if (head) {
         ElemParams o = ep;
         o.ln_w = c->w[W_LNOW];
         o.ln_b = c->w[W_LNOB];
         o.xo[0] = c->xo;
+        o.part = c->px;
+        o.nsplit = px_splits;
+        o.split_stride = xstride;
         pb(P_LN_OUT);
         launch_ln_out(o, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_out launch: %s", cudaGetErrorString(e));
-        Seg gh[1] = {{W_HEAD, A_XO, c->xo, d, EPI_F32, c->logits, c->V, nullptr}};
+        Seg gh[1] = {{W_HEAD, A_XO, c->xo, d, EPI_F32, c->logits, c->V, nullptr, 1}};
         pb(P_GEMM_HEAD);
         if ((rc = run_gemm(c, 0, gh, 1, B, nullptr, nullptr, lc, mode))) return rc;
         pe();
@@ -463,14 +538,15 @@ int enqueue_step(rwkv7_ctx *c, int B, bool head, bool sample, int mode, Prof *pf
 }
 
 int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
-    if (c->mode != 0) return enqueue_step(c, B, head, sample, c->mode);
+    if (c->mode != 0) return enqueue_step(c, c->stream, B, head, sample, c->mode);
     auto key = std::make_tuple(B, (int)head, (int)sample, c->mode);
     auto it = c->graphs.find(key);
     if (it == c->graphs.end()) {
         cudaGraph_t g = nullptr;
-        CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-        int rc = enqueue_step(c, B, head, sample, 0);
-        cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+        if (!c->cap_stream) CK(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
+        CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+        int rc = enqueue_step(c, c->cap_stream, B, head, sample, 0);
+        cudaError_t e2 = cudaStreamEndCapture(c->cap_stream, &g);
         if (rc) {
             if (g) cudaGraphDestroy(g);
             return rc;
@@ -574,12 +650,13 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
     shp(L_WR, d, d); shp(L_WK, d, d); shp(L_WV, d, d); shp(L_WO, d, d);
     shp(L_FK, F, d); shp(L_FV, d, F);
     c->wset.assign((size_t)W_COUNT * L, 0);
+    static const int tc_kinds[] = {L_WR, L_WK, L_WV, L_W1, L_A1, L_V1, L_G1, L_W2, L_A2, L_V2, L_G2, L_WO, L_FK, L_FV, W_HEAD};
+    for (int k : tc_kinds) c->tiled[k] = true;
     for (int k = 0; k < W_COUNT; ++k) {
         const size_t layers = per_layer(k) ? L : 1;
-        if ((rc = dalloc(c, &c->w[k], layers * c->wrows[k] * c->wcols[k]))) return bad(rc);
+        if ((rc = dalloc(c, &c->w[k], layers * layer_elems(c, k)))) return bad(rc);
         c->n_missing += layers;
     }
-    static const int tc_kinds[] = {L_WR, L_WK, L_WV, L_W1, L_A1, L_V1, L_G1, L_W2, L_A2, L_V2, L_G2, L_WO, L_FK, L_FV, W_HEAD};
     for (int k : tc_kinds)
         if ((rc = make_wmap(c, k))) return bad(rc);
     const size_t ns = c->n_slots;
@@ -620,9 +697,12 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
     if ((rc = dalloc(c, &c->nz, (size_t)F / 64 + 64))) return bad(rc);
     if ((rc = dalloc(c, &c->slots, R)) || (rc = dalloc(c, &c->tokens, R)) || (rc = dalloc(c, &c->next, R)))
         return bad(rc);
-    c->ws_floats = (size_t)c->nsm * 2 * R * GEMM_TILE_M;
-    if ((rc = dalloc(c, &c->ws, c->ws_floats))) return bad(rc);
-    if ((rc = dalloc(c, &c->counters, 4096))) return bad(rc);
+    const size_t SR = (size_t)MAX_SPLIT * R;
+    if ((rc = dalloc(c, &c->pr, SR * d)) || (rc = dalloc(c, &c->pk, SR * d)) || (rc = dalloc(c, &c->pv, SR * d)) ||
+        (rc = dalloc(c, &c->px, SR * d)) || (rc = dalloc(c, &c->phw, SR * c->rw)) ||
+        (rc = dalloc(c, &c->pha, SR * c->ra)) || (rc = dalloc(c, &c->phv, SR * c->rv)) ||
+        (rc = dalloc(c, &c->phg, SR * c->rg)))
+        return bad(rc);
     if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
     const int mk[6] = {A_XR, A_XW, A_XK, A_XV, A_XA, A_XG};
     for (int q = 0; q < 6; ++q)
@@ -642,6 +722,7 @@ void rwkv7_destroy(rwkv7_ctx *c) {
     cudaStreamSynchronize(c->stream);
     for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second);
     for (cudaEvent_t ev : c->prof.ev) cudaEventDestroy(ev);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     for (void *p : c->allocs) cudaFree(p);
     delete c;
 }
@@ -655,7 +736,23 @@ int rwkv7_set_weight(rwkv7_ctx *c, const char *name, const void *host_f16, size_
     if (parse_name(c, name, &kind, &layer)) return fail(c, RWKV7_ESHAPE, "unknown weight name '%s'", name);
     const size_t n = (size_t)c->wrows[kind] * c->wcols[kind];
     if (bytes != n * 2) return fail(c, RWKV7_ESHAPE, "'%s': %zu bytes given, %zu expected", name, bytes, n * 2);
-    CK(cudaMemcpy(c->w[kind] + (size_t)layer * n, host_f16, bytes, cudaMemcpyHostToDevice));
+    if (c->tiled[kind]) {
+        // repack [rows][cols] into zero-padded 128 x 64 tiles, tile order (row tile, k-block)
+        const int rows = c->wrows[kind], cols = c->wcols[kind], kb = kblocks(c, kind);
+        std::vector<__half> t(layer_elems(c, kind), __float2half(0.0f));
+        const __half *src = (const __half *)host_f16;
+        for (int r = 0; r < rows; ++r)
+            for (int k0 = 0; k0 < cols; k0 += GEMM_TILE_K) {
+                const int nk = std::min(GEMM_TILE_K, cols - k0);
+                __half *dst = t.data() + (((size_t)(r / GEMM_TILE_M) * kb + k0 / GEMM_TILE_K) * GEMM_TILE_M +
+                                          (r % GEMM_TILE_M)) * GEMM_TILE_K;
+                memcpy(dst, src + (size_t)r * cols + k0, (size_t)nk * sizeof(__half));
+            }
+        CK(cudaMemcpy(c->w[kind] + (size_t)layer * t.size(), t.data(), t.size() * sizeof(__half),
+                      cudaMemcpyHostToDevice));
+    } else {
+        CK(cudaMemcpy(c->w[kind] + (size_t)layer * n, host_f16, bytes, cudaMemcpyHostToDevice));
+    }
     uint8_t &f = c->wset[(size_t)kind * c->L + layer];
     if (!f) {
         f = 1;
@@ -926,7 +1023,7 @@ int rwkv7_set_mode(rwkv7_ctx *c, int32_t mode) {
 int32_t rwkv7_step_kernel_count(const rwkv7_ctx *c, int32_t B, int32_t with_sampling) {
     if (!c || B < 1) return 0;
     const int sub = (B + MAX_B - 1) / MAX_B;
-    return sub * (1 + 8 * c->L + 2 + (with_sampling ? 1 : 0));
+    return sub * (1 + 9 * c->L + 2 + (with_sampling ? 1 : 0));
 }
 
 int rwkv7_profile_step(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_tokens, int32_t B,
@@ -943,7 +1040,7 @@ int rwkv7_profile_step(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_to
     pf.n = 0;
     pf.cls.clear();
     const int mode = c->mode == 2 ? 2 : 1;
-    if ((rc = enqueue_step(c, B, true, with_sampling != 0, mode, &pf))) return rc;
+    if ((rc = enqueue_step(c, c->stream, B, true, with_sampling != 0, mode, &pf))) return rc;
     CK(cudaStreamSynchronize(c->stream));
     for (int i = 0; i < n_classes; ++i) {
         ms_out[i] = 0.0f;
