@@ -58,7 +58,7 @@ def class_bytes(dm: synth.Dims, B: int):
     return {
         "embed": B * d * (f16 + f32),
         "ln_mix": L * B * d * (f32 + 2 * f32 + 6 * f16) + L * B * d * (f32 + 2 * f32 + f16),
-        "gemm_proj": L * ((3 * d * d + d * rs) * f16 + B * 6 * d * f16 + B * (3 * d * f32 + rs * f16)),
+        "gemm_proj": L * ((3 * d * d + d * rs) * f16 + B * 6 * d * f16 + B * (3 * d + rs) * f32),
         "gemm_lora": L * (d * rs * f16 + B * rs * f16 + B * 4 * d * f32),
         "wkv": L * B * (H * 64 * 64 * f32 * 2 + 9 * d * f32 + d * f16),
         "gemm_out": L * (d * d * f16 + B * d * f16 + 2 * B * d * f32),
@@ -284,7 +284,7 @@ def main():
     prof = ctx.profile_step(slots, tokens, with_sampling=True)
     cb = class_bytes(dm, B)
     peak, peak_kind = _peaks()
-    gemm_cls = [k for k in prof if k.startswith("gemm")]
+    gemm_cls = [k for k in prof if k.startswith("gemm") and k in cb]
     gemm_ms = sum(prof[k][0] for k in gemm_cls)
     gemm_n = sum(prof[k][1] for k in gemm_cls)
     gemm_bytes = sum(cb[k] for k in gemm_cls)

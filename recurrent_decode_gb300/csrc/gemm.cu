@@ -54,33 +54,95 @@ __device__ __forceinline__ bool epi_store(const GemmSeg &s, int n, int b, float 
     return false;
 }
 
-// Epilogue of 16 consecutive slot rows b0..b0+15 of weight row n for split j:
-// the segment's epilogue when it is not split, else the raw fp32 partial.
-__device__ __forceinline__ bool epi_chunk(const GemmSeg &s, int n, int j, int b0, const float (&v)[16], int B) {
-    if (n >= s.rows) return false;
-    if (s.S > 1) {
-        float *out = (float *)s.out + (size_t)j * s.split_stride;
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (b0 + q < B) out[(size_t)(b0 + q) * s.ldo + n] = v[q];
-        return false;
-    }
-    if (s.epi == EPI_RESID) {
-        float *out = (float *)s.out;
-        float old[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) old[q] = (b0 + q < B) ? out[(size_t)(b0 + q) * s.ldo + n] : 0.0f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-            if (b0 + q < B) out[(size_t)(b0 + q) * s.ldo + n] = old[q] + v[q];
-        return false;
-    }
-    const float bias = (s.bias != nullptr) ? __half2float(s.bias[n]) : 0.0f;
+// Epilogue of one finished accumulator (one weight row n per thread, npad slot
+// columns in TMEM): the kind is dispatched once, then a straight-line loop per
+// 32-column chunk.  Split items store raw fp32 partials (slab `split`).  Every
+// lane executes the TMEM loads (they are warp-collective); stores are guarded.
+template <int KIND>
+__device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split, int npad,
+                                        int B) {
+    const bool live = n < sg.rows;
+    float bias = 0.0f;
+    if ((KIND == EPI_DECAY || KIND == EPI_SIGMOID_BIAS) && live) bias = __half2float(sg.bias[n]);
     bool nz = false;
+    for (int cb = 0; cb < npad; cb += 32) {
+        float v[32];
+        if (valid) {
+            if (cb + 32 <= npad) {
+                tmem_ld32(taddr + (uint32_t)cb, v);
+            } else {
+                float h[16];
+                tmem_ld16(taddr + (uint32_t)cb, h);
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-        if (b0 + q < B) nz |= epi_store(s, n, b0 + q, v[q], bias);
+                for (int q = 0; q < 16; ++q) {
+                    v[q] = h[q];
+                    v[q + 16] = 0.0f;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = 0.0f;
+        }
+        if (!live) continue;
+        const int nq = min(32, B - cb);
+        if (KIND == -1) {  // raw fp32 partial
+            float *out = (float *)sg.out + (size_t)split * sg.split_stride + (size_t)cb * sg.ldo + n;
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+                if (q < nq) out[(size_t)q * sg.ldo] = v[q];
+        } else if (KIND == EPI_RESID) {
+            float *out = (float *)sg.out + (size_t)cb * sg.ldo + n;
+            float old[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) old[q] = q < nq ? out[(size_t)q * sg.ldo] : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+                if (q < nq) out[(size_t)q * sg.ldo] = old[q] + v[q];
+        } else if (KIND == EPI_F32 || KIND == EPI_DECAY || KIND == EPI_SIGMOID_BIAS) {
+            float *out = (float *)sg.out + (size_t)cb * sg.ldo + n;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                float y = v[q];
+                if (KIND == EPI_DECAY) y = expf(-0.606530659712633f * sigm(bias + y));
+                if (KIND == EPI_SIGMOID_BIAS) y = sigm(bias + y);
+                if (q < nq) out[(size_t)q * sg.ldo] = y;
+            }
+        } else {  // fp16 outputs
+            __half *out = (__half *)sg.out + (size_t)cb * sg.ldo + n;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                float y = v[q];
+                if (KIND == EPI_F16_TANH) y = tanhf(y);
+                if (KIND == EPI_F16_SIGMOID) y = sigm(y);
+                if (KIND == EPI_RELU2) {
+                    y = fmaxf(y, 0.0f);
+                    y = y * y;
+                }
+                const __half hy = __float2half_rn(y);
+                if (q < nq) {
+                    out[(size_t)q * sg.ldo] = hy;
+                    if (KIND == EPI_RELU2) nz |= __half2float(hy) != 0.0f;
+                }
+            }
+        }
+    }
     return nz;
+}
+
+__device__ __forceinline__ bool epi_item(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split, int npad,
+                                         int B) {
+    if (sg.S > 1) return epi_run<-1>(sg, taddr, valid, n, split, npad, B);
+    switch (sg.epi) {
+        case EPI_F32: return epi_run<EPI_F32>(sg, taddr, valid, n, split, npad, B);
+        case EPI_F16: return epi_run<EPI_F16>(sg, taddr, valid, n, split, npad, B);
+        case EPI_F16_TANH: return epi_run<EPI_F16_TANH>(sg, taddr, valid, n, split, npad, B);
+        case EPI_F16_SIGMOID: return epi_run<EPI_F16_SIGMOID>(sg, taddr, valid, n, split, npad, B);
+        case EPI_DECAY: return epi_run<EPI_DECAY>(sg, taddr, valid, n, split, npad, B);
+        case EPI_SIGMOID_BIAS: return epi_run<EPI_SIGMOID_BIAS>(sg, taddr, valid, n, split, npad, B);
+        case EPI_RESID: return epi_run<EPI_RESID>(sg, taddr, valid, n, split, npad, B);
+        case EPI_RELU2: return epi_run<EPI_RELU2>(sg, taddr, valid, n, split, npad, B);
+        default: return false;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -307,17 +369,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
             const int nrow = it.tile * GEMM_TILE_M + row;
-            bool nzany = false;
-            for (int cb = 0; cb < npad; cb += 16) {
-                float v[16];
-                if (valid) {
-                    tmem_ld16(taddr + (uint32_t)cb, v);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-                }
-                nzany |= epi_chunk(sg, nrow, it.split, cb, v, B);
-            }
+            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B);
             tc_fence_before();
             mbar_arrive(&acc_empty[buf]);
             if (sg.epi == EPI_RELU2 && sg.S == 1 && nz_out != nullptr) {

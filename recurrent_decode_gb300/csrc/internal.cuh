@@ -108,17 +108,18 @@ void launch_embed(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
 void launch_ln_mix(const ElemParams &p, int nmix, const LaunchCfg &lc, cudaError_t *e);
 void launch_ln_out(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
 
+
 struct WkvParams {
     int B, d, H, n_slots, layer;
     const int32_t *slots;
-    const float *r, *k, *v;                      // partial slabs [nsplit][.][d]
+    const float *r, *k, *v;          // projection partial slabs [nsplit][bcap][d]
     int nsplit;
     long long split_stride;
-    const float *dec, *a, *vg, *g;               // [B][d]
-    float *v_first;                              // [B][d]
+    const float *dec, *a, *vg, *g;   // gates from the LoRA-up projection, [B][d]
+    float *v_first;                  // [B][d]
     const __half *k_k, *k_a, *r_k, *lnx_w, *lnx_b;
-    float *wkv;                                  // this layer's states [n_slots][H][64][64]
-    __half *z;                                   // [B][d]
+    float *wkv;                      // this layer's states [n_slots][H][64][64]
+    __half *z;                       // [B][d]
     uint32_t *err;
 };
 void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e);
@@ -232,6 +233,21 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Contiguous bulk copies between global and shared memory (16-byte aligned,
+// size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
@@ -300,8 +316,8 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                      smem_u32(bar))
                  : "memory");
 }
-// 32 lanes x 16 columns of 32-bit accumulator words: lane i of the warp gets
-// TMEM lane (base lane + i), columns [col, col + 16).
+// 32 lanes x 16 / 32 columns of 32-bit accumulator words: lane i of the warp
+// gets TMEM lane (base lane + i), columns [col, col + 16 / 32).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
@@ -313,6 +329,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile stored as rows of
