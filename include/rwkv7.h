@@ -132,6 +132,59 @@ RWKV7_API int rwkv7_decode_step_host(rwkv7_ctx *ctx, const int32_t *h_slots, con
 RWKV7_API int rwkv7_sample_batch(rwkv7_ctx *ctx, const int32_t *d_slots, const float *d_logits,
                        int32_t B, int32_t *d_next_out);
 
+/* Largest B * V that rwkv7_sample_rows_static accepts: 4,194,304 fp32 elements
+ * (16 MiB), e.g. 64 rows of a 65,536-token vocabulary. */
+#define RWKV7_SAMPLE_STATIC_MAX_ELEMS (1 << 22)
+
+/* Allocation-free variant of rwkv7_sample_batch.  The paper has no counterpart:
+ * it is a library convenience for callers that must not allocate device memory
+ * while they sample -- a serving process that has already handed all of HBM to
+ * its own arena (so cudaMalloc would fail), or a loop that cannot afford the
+ * device-wide synchronisation that cudaMalloc / cudaFree may cause, stalling
+ * the decode stream of every other batch.  It needs no rwkv7_ctx (whose
+ * creation allocates a whole slot pool): the caller owns every input and
+ * output, and the sampler's penalised-logit scratch lives in a fixed 16 MiB
+ * array of the library's device code, which the CUDA runtime reserves on every
+ * device that loads the library and keeps until the process exits.  The call
+ * makes no cudaMalloc / cudaFree and calls no allocating library routine.
+ *
+ * It runs the same kernel, with the same arithmetic, as rwkv7_sample_batch, so
+ * given equal logits, parameters, occurrence counts and draw counters both
+ * return the same tokens.
+ *
+ *  d_logits    device fp32 [B][V], row b = the logits of batch row b
+ *  d_rows      device int32 [B]: row b samples with per-sequence entry d_rows[b]
+ *              of the three arrays below (distinct within one call; an index
+ *              outside [0, n_rows) sets flag 1 in *d_err and gives token 0)
+ *  B, V        1 <= B, 1 <= V, B * V <= RWKV7_SAMPLE_STATIC_MAX_ELEMS; larger
+ *              batches are rejected (RWKV7_EINVAL) and must be split by the caller
+ *  n_rows      entries in each per-sequence array
+ *  d_occ       device fp32 [n_rows][V] occurrence counts, read and updated
+ *  d_params    device rwkv7_sampling [n_rows] (8-byte aligned), read only
+ *  d_ndraw     device uint64 [n_rows] draw counters (8-byte aligned), read and
+ *              incremented once per sampled (non-greedy) row
+ *  d_next_out  device int32 [B], the sampled tokens
+ *  d_err       device uint32 word; flags are OR-ed into it (1 = row index out of
+ *              range, 16 = no token could be kept); the caller clears it
+ *  cuda_stream the cudaStream_t to launch on (NULL = legacy default stream)
+ *  err_msg     if not NULL, receives a static text describing a host-side error
+ *              ("" on success); valid until the next call from the same thread
+ *
+ * Set-up: the first call on each device (with that device current) looks up the
+ * scratch array's device address and sets the kernel's shared-memory limit;
+ * make that first call before any stream capture on that device.
+ * Scratch contents: nothing in it has to start at zero -- each call writes
+ * every element it later reads -- and it keeps the last call's values.  All
+ * calls on a device share the one array, so two calls whose kernels overlap on
+ * the GPU (different streams, or different host threads without ordering)
+ * race on it and may return wrong tokens; order them on one stream.
+ * Asynchronous on cuda_stream; returns RWKV7_OK, RWKV7_EINVAL (null pointer,
+ * misaligned array, bad or too large size) or RWKV7_ECUDA. */
+RWKV7_API int rwkv7_sample_rows_static(const float *d_logits, const int32_t *d_rows, int32_t B, int32_t V,
+                                       int32_t n_rows, float *d_occ, const rwkv7_sampling *d_params,
+                                       uint64_t *d_ndraw, int32_t *d_next_out, uint32_t *d_err,
+                                       void *cuda_stream, const char **err_msg);
+
 /* Wait for the ctx's stream and report device-side errors latched since the
  * last call (RWKV7_EINVAL for bad slots/tokens, RWKV7_ETIMEOUT for a bounded
  * wait that gave up).  Clears the latched error. */

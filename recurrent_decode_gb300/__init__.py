@@ -58,6 +58,9 @@ SIGNATURES = {
     "rwkv7_decode_step": (C.c_int, [_VP, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "rwkv7_decode_step_host": (C.c_int, [_VP, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     "rwkv7_sample_batch": (C.c_int, [_VP, C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
+    "rwkv7_sample_rows_static": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+                                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.POINTER(C.c_char_p)]),
     "rwkv7_synchronize": (C.c_int, [_VP]),
     "rwkv7_set_mode": (C.c_int, [_VP, C.c_int32]),
     "rwkv7_get_io_buffers": (C.c_int, [_VP, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
@@ -66,6 +69,8 @@ SIGNATURES = {
     "rwkv7_profile_step": (C.c_int, [_VP, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
                                      C.c_void_p, C.c_int32]),
 }
+
+SAMPLE_STATIC_MAX_ELEMS = 1 << 22
 
 PROF_CLASSES = ["embed", "ln_mix", "gemm_proj", "gemm_lora", "wkv", "gemm_out", "gemm_key", "gemm_value",
                 "ln_out", "gemm_head", "sampler"]
@@ -98,6 +103,47 @@ def _ptr(t, dtype, what):
     if t.dtype != dtype or not t.is_contiguous():
         raise TypeError(f"{what} must be a contiguous {dtype} tensor")
     return C.c_void_p(t.data_ptr())
+
+
+def sampling_table(params) -> np.ndarray:
+    """Pack a list of sampling-parameter dicts (keys of Rwkv7.set_sampling) into
+    the byte image of an rwkv7_sampling array, ready to copy to the device for
+    sample_rows_static."""
+    arr = (Sampling * len(params))()
+    for i, p in enumerate(params):
+        q = dict(temperature=1.0, top_p=0.3, top_k=0, presence=0.0, frequency=1.0, penalty_decay=0.996,
+                 seed=0, greedy=False)
+        q.update(p)
+        arr[i] = Sampling(q["temperature"], q["top_p"], q["top_k"], q["presence"], q["frequency"],
+                          q["penalty_decay"], q["seed"], int(bool(q["greedy"])))
+    return np.frombuffer(bytes(arr), dtype=np.uint8).copy()
+
+
+def sample_rows_static(logits, rows, occ, params, ndraw, next_out, err, stream=None):
+    """rwkv7_sample_rows_static: sample one token per row of logits [B][V] with
+    the per-sequence entries rows[b] of occ [n_rows][V] fp32, params (uint8
+    device image of an rwkv7_sampling array, see sampling_table) and ndraw
+    [n_rows] int64 (the uint64 draw counters), writing next_out [B] int32 and
+    OR-ing error flags into err [1] int32.  The library allocates nothing for
+    this call; its scratch is a fixed 16 MiB device array, so B * V must not
+    exceed SAMPLE_STATIC_MAX_ELEMS.  stream: torch.cuda.Stream or None (current)."""
+    import torch
+    lib = load_library()
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    n_rows = int(occ.shape[0])
+    if params.dtype != torch.uint8 or params.numel() != n_rows * C.sizeof(Sampling):
+        raise TypeError("params must be a uint8 tensor holding n_rows rwkv7_sampling records")
+    if logits.dim() != 2 or occ.dim() != 2 or occ.shape[1] != V or rows.numel() != B \
+            or next_out.numel() != B or ndraw.numel() != n_rows or err.numel() != 1:
+        raise ValueError("shapes: logits [B][V], rows [B], occ [n_rows][V], ndraw [n_rows], next_out [B], err [1]")
+    st = stream if stream is not None else torch.cuda.current_stream()
+    msg = C.c_char_p()
+    rc = lib.rwkv7_sample_rows_static(_ptr(logits, torch.float32, "logits"), _ptr(rows, torch.int32, "rows"), B, V,
+                                      n_rows, _ptr(occ, torch.float32, "occ"), _ptr(params, torch.uint8, "params"),
+                                      _ptr(ndraw, torch.int64, "ndraw"), _ptr(next_out, torch.int32, "next_out"),
+                                      _ptr(err, torch.int32, "err"), C.c_void_p(st.cuda_stream), C.byref(msg))
+    if rc != OK:
+        raise RWKV7Error(rc, (msg.value or b"").decode())
 
 
 class Rwkv7:

@@ -16,6 +16,12 @@
 //   token = first kept index whose running qT sum exceeds r; then
 //   occ *= penalty_decay, occ[token] += 1.
 // greedy: argmax of the raw logits, lowest index on ties.
+#include <cstddef>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/rwkv7.h"
 #include "internal.cuh"
 
 namespace rk {
@@ -380,3 +386,106 @@ void launch_sampler(const SamplerParams &p, const LaunchCfg &lc, cudaError_t *e)
 }
 
 }  // namespace rk
+
+// ---------------------------------------------------------------------------
+// rwkv7_sample_rows_static: the sampler above for callers that must not
+// allocate device memory (a process whose HBM already belongs to its own
+// arena, or a serving loop that cannot take the device-wide synchronisation
+// cudaMalloc / cudaFree may cause).  The penalised-logit scratch the kernel
+// needs ([B][V] fp32) comes from this fixed module array instead of a ctx
+// buffer; the CUDA runtime reserves it on each device that loads the library
+// and keeps it until the process exits.  The kernel and its arithmetic are the
+// ones rwkv7_sample_batch launches.
+namespace {
+
+constexpr size_t STATIC_LPEN_ELEMS = (size_t)RWKV7_SAMPLE_STATIC_MAX_ELEMS;  // 16 MiB of fp32
+constexpr int STATIC_MAX_DEVICES = 64;
+
+// The scratch array.  In host code this name is only a stand-in for the device
+// symbol: its device address comes from cudaGetSymbolAddress, per device.
+static __device__ __align__(256) float g_static_lpen[STATIC_LPEN_ELEMS];
+
+std::mutex g_static_mu;
+float *g_static_lpen_dev[STATIC_MAX_DEVICES] = {};  // device address of g_static_lpen, per device
+thread_local char g_static_msg[192];
+
+// The public parameter struct is handed to the kernel as its device copy.
+static_assert(sizeof(rwkv7_sampling) == sizeof(rk::SampleParamsDev), "sampling struct size");
+static_assert(offsetof(rwkv7_sampling, top_k) == offsetof(rk::SampleParamsDev, top_k), "top_k offset");
+static_assert(offsetof(rwkv7_sampling, penalty_decay) == offsetof(rk::SampleParamsDev, penalty_decay),
+              "penalty_decay offset");
+static_assert(offsetof(rwkv7_sampling, seed) == offsetof(rk::SampleParamsDev, seed), "seed offset");
+static_assert(offsetof(rwkv7_sampling, greedy) == offsetof(rk::SampleParamsDev, greedy), "greedy offset");
+
+int static_fail(const char **err_msg, int code, const char *fmt, long long a = 0, long long b = 0) {
+    snprintf(g_static_msg, sizeof g_static_msg, fmt, a, b);
+    if (err_msg) *err_msg = g_static_msg;
+    return code;
+}
+
+// Once per device, with that device current: look up the scratch's device
+// address and allow the kernel its dynamic shared memory on this device.
+int static_setup(float **lpen, const char **err_msg) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return static_fail(err_msg, RWKV7_ECUDA, "cudaGetDevice failed (error %lld)", (long long)e);
+    if (dev < 0 || dev >= STATIC_MAX_DEVICES)
+        return static_fail(err_msg, RWKV7_EINVAL, "device ordinal %lld beyond the supported %lld", dev,
+                           STATIC_MAX_DEVICES);
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_lpen_dev[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_lpen);
+        if (e != cudaSuccess || !p)
+            return static_fail(err_msg, RWKV7_ECUDA, "cudaGetSymbolAddress of the sampler scratch failed (error %lld)",
+                               (long long)e);
+        e = cudaFuncSetAttribute(rk::sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(rk::SmpShared));
+        if (e != cudaSuccess)
+            return static_fail(err_msg, RWKV7_ECUDA, "setting the sampler's shared-memory limit failed (error %lld)",
+                               (long long)e);
+        g_static_lpen_dev[dev] = static_cast<float *>(p);
+    }
+    *lpen = g_static_lpen_dev[dev];
+    return RWKV7_OK;
+}
+
+}  // namespace
+
+extern "C" int rwkv7_sample_rows_static(const float *d_logits, const int32_t *d_rows, int32_t B, int32_t V,
+                                        int32_t n_rows, float *d_occ, const rwkv7_sampling *d_params,
+                                        uint64_t *d_ndraw, int32_t *d_next_out, uint32_t *d_err,
+                                        void *cuda_stream, const char **err_msg) {
+    if (err_msg) *err_msg = "";
+    if (!d_logits || !d_rows || !d_occ || !d_params || !d_ndraw || !d_next_out || !d_err)
+        return static_fail(err_msg, RWKV7_EINVAL, "null pointer argument");
+    if (((uintptr_t)d_params & 7u) || ((uintptr_t)d_ndraw & 7u))
+        return static_fail(err_msg, RWKV7_EINVAL, "d_params and d_ndraw must be 8-byte aligned");
+    if (B < 1 || V < 1 || n_rows < 1)
+        return static_fail(err_msg, RWKV7_EINVAL, "B, V and n_rows must be >= 1 (B=%lld, V=%lld)", B, V);
+    if ((size_t)B * (size_t)V > STATIC_LPEN_ELEMS)
+        return static_fail(err_msg, RWKV7_EINVAL,
+                           "B * V = %lld exceeds the static sampler scratch of %lld fp32 elements; split the batch",
+                           (long long)B * V, (long long)STATIC_LPEN_ELEMS);
+    float *lpen = nullptr;
+    int rc = static_setup(&lpen, err_msg);
+    if (rc) return rc;
+    rk::SamplerParams sp;
+    memset(&sp, 0, sizeof sp);
+    sp.B = B;
+    sp.V = V;
+    sp.n_slots = n_rows;
+    sp.slots = d_rows;
+    sp.logits = d_logits;
+    sp.occ = d_occ;
+    sp.params = reinterpret_cast<const rk::SampleParamsDev *>(d_params);
+    sp.ndraw = reinterpret_cast<unsigned long long *>(d_ndraw);
+    sp.lpen = lpen;  // rows b use [b*V, (b+1)*V), inside the array since B*V <= its size
+    sp.next = d_next_out;
+    sp.err = d_err;
+    cudaError_t e = cudaSuccess;
+    rk::launch_sampler(sp, rk::LaunchCfg{static_cast<cudaStream_t>(cuda_stream), false}, &e);
+    if (e != cudaSuccess)
+        return static_fail(err_msg, RWKV7_ECUDA, "sampler launch failed (error %lld)", (long long)e);
+    return RWKV7_OK;
+}
