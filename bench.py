@@ -67,6 +67,7 @@ def class_bytes(dm: synth.Dims, B: int):
         "ln_out": B * d * (f32 + f16),
         "gemm_head": V * d * f16 + B * d * f16 + B * V * f32,
         "sampler": B * V * f32,
+        "lora_fin": L * B * rs * (f32 + f16),
     }
 
 
@@ -152,7 +153,7 @@ def run_reference(args, wl, dm):
     if rank != 0:
         return 0
     import oracle
-    weights = synth.make_weights(wl["shape"])
+    weights = synth.make_weights(wl["shape"], n_layer=dm.n_layer)
     threads = os.cpu_count() or 1
     oracle.set_threads(threads)
     m = oracle.Model(weights, dm)
@@ -181,7 +182,7 @@ def run_reference(args, wl, dm):
 def _config(wl, dm, args):
     return {"workload": f"RWKV-7 {dm.name} shape batched greedy decode" if wl.get("greedy")
             else f"RWKV-7 {dm.name} shape batched sampled decode (top_p {wl.get('top_p')})",
-            "shape": dm.name, "B": wl["B"], "prompt_tokens": wl["prompt"], "decode_steps_timed": args.steps,
+            "shape": dm.name, "n_layer": dm.n_layer, "B": wl["B"], "prompt_tokens": wl["prompt"], "decode_steps_timed": args.steps,
             "weights": "random-init fp16 (seed 0)", "state": "fp32",
             "l2": "inputs larger than L2 (weights + states per step >> 126 MB), no flush"}
 
@@ -196,10 +197,15 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run a model with this many layers of the shape's sizes")
+    ap.add_argument("--prompt", type=int, default=0, help="profiling only: override the prompt length")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    wl = synth.WORKLOADS[args.config]
-    dm = synth.Dims(wl["shape"])
+    wl = dict(synth.WORKLOADS[args.config])
+    if args.prompt:
+        wl["prompt"] = max(2, args.prompt)
+    dm = synth.Dims(wl["shape"], args.layers or None)
     if args.impl == "reference":
         return run_reference(args, wl, dm)
 
@@ -215,7 +221,7 @@ def main():
     import recurrent_decode_gb300 as rd
 
     B = wl["B"]
-    weights = synth.make_weights(wl["shape"])
+    weights = synth.make_weights(wl["shape"], n_layer=args.layers or None)
     ctx = rd.Rwkv7(dm, B)
     ctx.set_weights(weights)
     for s in range(B):

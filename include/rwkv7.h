@@ -212,7 +212,8 @@ RWKV7_API int rwkv7_get_io_buffers(rwkv7_ctx *ctx, int32_t **d_slots, int32_t **
 #define RWKV7_PROF_LN_OUT 8      /* final LayerNorm */
 #define RWKV7_PROF_GEMM_HEAD 9   /* head projection to fp32 logits */
 #define RWKV7_PROF_SAMPLER 10    /* penalties + sampling */
-#define RWKV7_PROF_CLASSES 11
+#define RWKV7_PROF_LORA_FIN 11   /* LoRA-down split sums + tanh / sigmoid to fp16 hidden */
+#define RWKV7_PROF_CLASSES 12
 
 /* Run one step of B <= min(n_slots, 256) slots with every kernel launched
  * directly (no graph, no dependent-launch overlap) and bracketed by CUDA events

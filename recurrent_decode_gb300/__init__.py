@@ -73,7 +73,7 @@ SIGNATURES = {
 SAMPLE_STATIC_MAX_ELEMS = 1 << 22
 
 PROF_CLASSES = ["embed", "ln_mix", "gemm_proj", "gemm_lora", "wkv", "gemm_out", "gemm_key", "gemm_value",
-                "ln_out", "gemm_head", "sampler"]
+                "ln_out", "gemm_head", "sampler", "lora_fin"]
 
 _lib = None
 

@@ -51,7 +51,7 @@ const char *kind_name[W_COUNT] = {
 
 // kernel classes reported by rwkv7_profile_step
 enum PClass { P_EMBED, P_LN_MIX, P_GEMM_PROJ, P_GEMM_LORA, P_WKV, P_GEMM_OUT, P_GEMM_KEY, P_GEMM_VALUE, P_LN_OUT,
-              P_GEMM_HEAD, P_SAMPLER, P_COUNT };
+              P_GEMM_HEAD, P_SAMPLER, P_LORA_FIN, P_COUNT };
 
 struct Prof {
     std::vector<cudaEvent_t> ev;  // pairs (begin, end)
@@ -420,7 +420,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         lf.out[0] = c->hw; lf.out[1] = c->ha; lf.out[2] = c->hv; lf.out[3] = c->hg;
         lf.act[0] = 1; lf.act[1] = 0; lf.act[2] = 0; lf.act[3] = 2;
         lf.bcap = c->bcap;
-        pb(P_GEMM_LORA);
+        pb(P_LORA_FIN);
         launch_lora_fin(lf, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "lora_fin launch: %s", cudaGetErrorString(e));

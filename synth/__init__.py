@@ -58,10 +58,12 @@ _CHUNK = 1 << 22  # elements per independent RNG stream (fixed: results do not d
 class Dims:
     """Model dimensions of one named shape."""
 
-    def __init__(self, name: str):
-        n_layer, d, f, v, lora = SHAPES[name]
+    def __init__(self, name: str, n_layer: int | None = None):
+        """n_layer, if given, replaces the shape's layer count (a shorter model
+        with the same per-layer sizes, for small profiling cases)."""
+        nl, d, f, v, lora = SHAPES[name]
         self.name = name
-        self.n_layer = n_layer
+        self.n_layer = int(n_layer) if n_layer else nl
         self.d_model = d
         self.head_size = HEAD_SIZE
         self.n_head = d // HEAD_SIZE
@@ -139,15 +141,16 @@ def _fill(out16: np.ndarray, init, seed: int, tid: int, c0: int, c1: int):
 
 
 def make_weights(shape: str, seed: int = WEIGHT_SEED, threads: int | None = None,
-                 overrides: dict | None = None):
+                 overrides: dict | None = None, n_layer: int | None = None):
     """Return {name: fp16 ndarray} for the named shape, drawn from `seed`.
 
     Every tensor (and every 4 Mi-element chunk of it) has its own PCG64 stream
     keyed by (seed, tensor index, chunk index), so the result is the same for any
     thread count.  `overrides` maps name -> callable(ndarray) that edits a tensor
     in place after drawing (used by tests that zero parts of the model).
+    `n_layer` shortens the model as in Dims.
     """
-    dims = Dims(shape)
+    dims = Dims(shape, n_layer)
     specs = tensor_specs(dims)
     out = {name: np.empty(shp, dtype=np.float16) for name, shp, _ in specs}
     jobs = []
