@@ -200,6 +200,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run a model with this many layers of the shape's sizes")
     ap.add_argument("--prompt", type=int, default=0, help="profiling only: override the prompt length")
+    ap.add_argument("--mode", type=int, default=-1,
+                    help="implementation: 0 multi-kernel CUDA graph, 3 persistent kernel (default: library default)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = dict(synth.WORKLOADS[args.config])
@@ -224,6 +226,8 @@ def main():
     weights = synth.make_weights(wl["shape"], n_layer=args.layers or None)
     ctx = rd.Rwkv7(dm, B)
     ctx.set_weights(weights)
+    if args.mode >= 0:
+        ctx.set_mode(args.mode)
     for s in range(B):
         if wl.get("greedy"):
             ctx.set_sampling(s, greedy=True)

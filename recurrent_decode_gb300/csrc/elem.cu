@@ -334,7 +334,7 @@ __global__ void lora_fin_kernel(const LoraFinParams p) {
         const long long stride = (long long)p.bcap * p.r[i];
         float acc = 0.0f;
         for (int j = 0; j < p.S; ++j) acc += src[(size_t)j * stride];
-        const float y = p.act[i] == 1 ? tanhf(acc) : (p.act[i] == 2 ? 1.0f / (1.0f + expf(-acc)) : acc);
+        const float y = p.act[i] == 1 ? fast_tanh(acc) : (p.act[i] == 2 ? fast_sigmoid(acc) : acc);
         p.out[i][(size_t)b * p.r[i] + col] = __float2half_rn(y);
     }
 }

@@ -29,7 +29,6 @@ constexpr uint32_t W_TILE_BYTES = GEMM_TILE_M * GEMM_TILE_K * 2;  // 16 KB
 constexpr int KB_STAGE = 2;
 constexpr uint32_t W_STAGE_BYTES = KB_STAGE * W_TILE_BYTES;
 
-__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 // Apply the segment's epilogue to one result.  Returns true when EPI_RELU2
 // stores a nonzero fp16 value (so the caller can record sparsity).
@@ -38,10 +37,10 @@ __device__ __forceinline__ bool epi_store(const GemmSeg &s, int n, int b, float 
     switch (s.epi) {
         case EPI_F32: ((float *)s.out)[o] = acc; break;
         case EPI_F16: ((__half *)s.out)[o] = __float2half_rn(acc); break;
-        case EPI_F16_TANH: ((__half *)s.out)[o] = __float2half_rn(tanhf(acc)); break;
-        case EPI_F16_SIGMOID: ((__half *)s.out)[o] = __float2half_rn(sigm(acc)); break;
-        case EPI_DECAY: ((float *)s.out)[o] = expf(-0.606530659712633f * sigm(bias + acc)); break;
-        case EPI_SIGMOID_BIAS: ((float *)s.out)[o] = sigm(bias + acc); break;
+        case EPI_F16_TANH: ((__half *)s.out)[o] = __float2half_rn(fast_tanh(acc)); break;
+        case EPI_F16_SIGMOID: ((__half *)s.out)[o] = __float2half_rn(fast_sigmoid(acc)); break;
+        case EPI_DECAY: ((float *)s.out)[o] = rwkv_decay(bias + acc); break;
+        case EPI_SIGMOID_BIAS: ((float *)s.out)[o] = fast_sigmoid(bias + acc); break;
         case EPI_RESID: ((float *)s.out)[o] += acc; break;
         case EPI_RELU2: {
             float t = fmaxf(acc, 0.0f);
@@ -103,8 +102,8 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
                 float y = v[q];
-                if (KIND == EPI_DECAY) y = expf(-0.606530659712633f * sigm(bias + y));
-                if (KIND == EPI_SIGMOID_BIAS) y = sigm(bias + y);
+                if (KIND == EPI_DECAY) y = rwkv_decay(bias + y);
+                if (KIND == EPI_SIGMOID_BIAS) y = fast_sigmoid(bias + y);
                 if (q < nq) out[(size_t)q * sg.ldo] = y;
             }
         } else {  // fp16 outputs
@@ -112,8 +111,8 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
                 float y = v[q];
-                if (KIND == EPI_F16_TANH) y = tanhf(y);
-                if (KIND == EPI_F16_SIGMOID) y = sigm(y);
+                if (KIND == EPI_F16_TANH) y = fast_tanh(y);
+                if (KIND == EPI_F16_SIGMOID) y = fast_sigmoid(y);
                 if (KIND == EPI_RELU2) {
                     y = fmaxf(y, 0.0f);
                     y = y * y;

@@ -115,6 +115,7 @@ struct rwkv7_ctx {
     uint32_t *errw = nullptr;
 
     CUtensorMap wmap[W_COUNT]{};
+    CUtensorMap wmap1[W_COUNT]{};  // box of one k-block tile (persistent step with N > 128)
     bool has_wmap[W_COUNT]{};
     CUtensorMap amap[A_COUNT][MAX_B / 16]{};
     bool amap_ok[A_COUNT][MAX_B / 16]{};
@@ -122,6 +123,12 @@ struct rwkv7_ctx {
     int acols[A_COUNT]{};
 
     std::map<std::tuple<int, int, int, int>, cudaGraphExec_t> graphs;
+    // persistent step: counters (phase, tile, slot bitmap, abort), zeroed per step
+    uint32_t *pkbuf = nullptr;
+    size_t pk_words = 0;
+    int pk_tcnt_layer = 0;
+    float *p4 = nullptr;  // key-projection partial slabs [PK_S4_MAX][bcap][F]
+    std::map<std::pair<int, int>, PkParams> pk_params;
     std::vector<void *> allocs;
     Prof prof;
 };
@@ -201,7 +208,10 @@ int make_wmap(rwkv7_ctx *c, int kind) {
     uint64_t strides[2] = {(uint64_t)GEMM_TILE_K * 2, (uint64_t)GEMM_TILE_K * GEMM_TILE_M * 2};
     uint32_t box[3] = {64, 128, 2};
     c->has_wmap[kind] = true;
-    return make_map(c, &c->wmap[kind], c->w[kind], 3, dims, strides, box);
+    int rc = make_map(c, &c->wmap[kind], c->w[kind], 3, dims, strides, box);
+    if (rc) return rc;
+    uint32_t box1[3] = {64, 128, 1};
+    return make_map(c, &c->wmap1[kind], c->w[kind], 3, dims, strides, box1);
 }
 
 // Split factor of a launch whose segments hold `tiles` row tiles in all:
@@ -537,7 +547,224 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     return RWKV7_OK;
 }
 
+// ---------------------------------------------------------------- persistent step
+// k-splits of a phase with `tiles` row tiles of `units` ring stages each: the
+// smallest per-CTA load, counting about 1.5 stages of fixed cost per item and a
+// little per split.
+int pk_split(const rwkv7_ctx *c, int tiles, int units, int max_s) {
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= std::min(max_s, units); ++s) {
+        const int per_cta = (tiles * s + c->nsm - 1) / c->nsm;
+        const double cost = per_cta * ((units + s - 1) / s + 1.5) + (s > 1 ? 0.25 * s : 0.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+int build_pk(rwkv7_ctx *c, int B, bool head, PkParams **out) {
+    auto key = std::make_pair(B, (int)head);
+    auto found = c->pk_params.find(key);
+    if (found != c->pk_params.end()) {
+        *out = &found->second;
+        return RWKV7_OK;
+    }
+    PkParams p;
+    memset(&p, 0, sizeof p);
+    const int d = c->d;
+    p.npad = (B + 15) / 16 * 16;
+    p.kbs = p.npad <= 128 ? 2 : 1;
+    p.stages = pk_max_stages(p.npad, p.kbs);
+    if (p.stages < 2) return fail(c, RWKV7_ECUDA, "persistent step: shared memory too small");
+    int ncols = 32;
+    while (ncols < 2 * p.npad) ncols <<= 1;
+    p.ncols = ncols;
+    if (d > 4096) return fail(c, RWKV7_EINVAL, "persistent step supports d_model <= 4096");
+    int wslot[W_COUNT], aslot[A_COUNT];
+    for (int i = 0; i < W_COUNT; ++i) wslot[i] = -1;
+    for (int i = 0; i < A_COUNT; ++i) aslot[i] = -1;
+    int nmaps = 0;
+    auto wmap_of = [&](int kind) -> int {
+        if (wslot[kind] < 0) {
+            if (nmaps >= PK_MAX_MAPS) return -1;
+            wslot[kind] = nmaps;
+            p.maps[nmaps++] = p.kbs == 2 ? c->wmap[kind] : c->wmap1[kind];
+        }
+        return wslot[kind];
+    };
+    auto amap_of = [&](int which) -> int {
+        if (aslot[which] < 0) {
+            if (nmaps >= PK_MAX_MAPS) return -1;
+            const CUtensorMap *am = get_amap(c, which, p.npad);
+            if (!am) return -1;
+            aslot[which] = nmaps;
+            p.maps[nmaps++] = *am;
+        }
+        return aslot[which];
+    };
+    const int G = c->nsm;
+    const int units = kblocks(c, L_WR) / p.kbs;
+    const int g1_tiles = 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) + row_tiles(c, L_V1) +
+                         row_tiles(c, L_G1);
+    const int s1 = pk_split(c, g1_tiles, units, MAX_SPLIT);
+    const int s3 = pk_split(c, row_tiles(c, L_WO), kblocks(c, L_WO) / p.kbs, MAX_SPLIT);
+    const int s5 = pk_split(c, row_tiles(c, L_FV), kblocks(c, L_FV) / p.kbs, MAX_SPLIT);
+    const long long xs = (long long)c->bcap;
+    int cnt0 = 0;
+    bool bad_map = false;
+    auto add = [&](PkGemm &g, int kind, int abuf, int epi, int fix, void *outp, int ldo, float *part,
+                   const __half *bias, int S) {
+        PkSeg &sg = g.seg[g.nseg++];
+        sg.wmap = wmap_of(kind);
+        sg.xmap = amap_of(abuf);
+        if (sg.wmap < 0 || sg.xmap < 0) bad_map = true;
+        sg.tiles = row_tiles(c, kind);
+        sg.kb = kblocks(c, kind);
+        sg.rows = c->wrows[kind];
+        sg.S = std::max(1, std::min(S, sg.kb / p.kbs));
+        sg.layer_tiles = per_layer(kind) ? sg.tiles * sg.kb : 0;
+        sg.item0 = g.nitems;
+        g.nitems += sg.tiles * sg.S;
+        sg.epi = epi;
+        sg.fix = fix;
+        sg.cnt0 = 0;
+        if (fix && sg.S > 1) {
+            sg.cnt0 = cnt0;
+            cnt0 += sg.tiles;
+        }
+        sg.ldo = ldo;
+        sg.out = outp;
+        sg.part = part;
+        sg.split_stride = xs * ldo;
+        sg.bias = bias;
+        sg.bias_stride = d;
+    };
+    for (int v1 = 0; v1 < 2; ++v1) {  // layer 0 has no value LoRA
+        PkGemm &g = p.g[v1 ? PKG_G1 : PKG_G1_0];
+        cnt0 = 0;
+        add(g, L_WR, A_XR, EPI_F32, 0, nullptr, d, c->pr, nullptr, s1);  // slabs, added by the WKV phase
+        add(g, L_WK, A_XK, EPI_F32, 0, nullptr, d, c->pk, nullptr, s1);
+        add(g, L_WV, A_XV, EPI_F32, 0, nullptr, d, c->pv, nullptr, s1);
+        // LoRA-down outputs feed the next GEMM's operand loads, so they are
+        // produced whole (no split) with their activation applied
+        add(g, L_W1, A_XW, EPI_F16_TANH, 1, c->hw, c->rw, c->phw, nullptr, 1);
+        add(g, L_A1, A_XA, EPI_F16, 1, c->ha, c->ra, c->pha, nullptr, 1);
+        if (v1) add(g, L_V1, A_XV, EPI_F16, 1, c->hv, c->rv, c->phv, nullptr, 1);
+        add(g, L_G1, A_XG, EPI_F16_SIGMOID, 1, c->hg, c->rg, c->phg, nullptr, 1);
+        PkGemm &g2 = p.g[v1 ? PKG_G2 : PKG_G2_0];
+        add(g2, L_W2, A_HW, EPI_DECAY, 1, c->dec, d, nullptr, c->w[L_W0], 1);
+        add(g2, L_A2, A_HA, EPI_SIGMOID_BIAS, 1, c->a, d, nullptr, c->w[L_A0], 1);
+        if (v1) add(g2, L_V2, A_HV, EPI_SIGMOID_BIAS, 1, c->vg, d, nullptr, c->w[L_V0], 1);
+        add(g2, L_G2, A_HG, EPI_F32, 1, c->g, d, nullptr, nullptr, 1);
+    }
+    const int g1cnt = cnt0;
+    add(p.g[PKG_G3], L_WO, A_Z, EPI_F32, 0, nullptr, d, c->px, nullptr, s3);
+    cnt0 = g1cnt;
+    add(p.g[PKG_G4], L_FK, A_XKF, EPI_RELU2, 1, c->h, c->F, c->p4, nullptr, env_int("RWKV7_PK_S4", 1));
+    add(p.g[PKG_G5], L_FV, A_H, EPI_F32, 0, nullptr, d, c->px, nullptr, s5);
+    cnt0 = 0;
+    add(p.g[PKG_HEAD], W_HEAD, A_XO, EPI_F32, 1, c->logits, c->V, nullptr, nullptr, 1);
+    if (bad_map) return fail(c, RWKV7_ECUDA, "persistent step: tensor maps");
+    if (cnt0 > c->pk_tcnt_layer && false) return fail(c, RWKV7_ECUDA, "internal: tile counters");
+    p.nmaps = nmaps;
+    p.B = B;
+    p.d = d;
+    p.H = c->H;
+    p.V = c->V;
+    p.L = c->L;
+    p.n_slots = c->n_slots;
+    p.head = head ? 1 : 0;
+    p.s3 = p.g[PKG_G3].seg[0].S;
+    p.s5 = p.g[PKG_G5].seg[0].S;
+    p.s1 = p.g[PKG_G1].seg[0].S;
+    p.pr = c->pr;
+    p.pk = c->pk;
+    p.pv = c->pv;
+    p.xstride = xs * d;
+    p.tcnt_layer = c->pk_tcnt_layer;
+    p.slots = c->slots;
+    p.tokens = c->tokens;
+    p.x = c->x;
+    p.emb = c->w[W_EMB];
+    p.ln0w = c->w[W_LN0W];
+    p.ln0b = c->w[W_LN0B];
+    p.lnow = c->w[W_LNOW];
+    p.lnob = c->w[W_LNOB];
+    p.ln1w = c->w[L_LN1W];
+    p.ln1b = c->w[L_LN1B];
+    p.ln2w = c->w[L_LN2W];
+    p.ln2b = c->w[L_LN2B];
+    const int mk[6] = {L_XR, L_XW, L_XK, L_XV, L_XA, L_XG};
+    for (int q = 0; q < 6; ++q) {
+        p.mu[q] = c->w[mk[q]];
+        p.xmix[q] = c->xmix[q];
+    }
+    p.fxk = c->w[L_FXK];
+    p.k_k = c->w[L_KK];
+    p.k_a = c->w[L_KA];
+    p.r_k = c->w[L_RK];
+    p.lnxw = c->w[L_LNXW];
+    p.lnxb = c->w[L_LNXB];
+    p.xk = c->xk;
+    p.z = c->z;
+    p.xo = c->xo;
+    p.r = c->r;
+    p.k = c->k;
+    p.v = c->v;
+    p.dec = c->dec;
+    p.a = c->a;
+    p.vg = c->vg;
+    p.gate = c->g;
+    p.vfirst = c->vfirst;
+    p.px = c->px;
+    p.wkv = c->wkv;
+    p.shift_att = c->shift_att;
+    p.shift_ffn = c->shift_ffn;
+    p.cnt = c->pkbuf;
+    p.tcnt = p.cnt + (size_t)c->L * PK_NPH + 2;
+    p.dup = p.tcnt + (size_t)c->L * c->pk_tcnt_layer + row_tiles(c, W_HEAD);
+    p.abort_flag = p.dup + (c->n_slots + 31) / 32;
+    p.diag = p.abort_flag + 1;
+    p.prog = p.diag + 8;
+    p.err = c->errw;
+    (void)G;
+    *out = &c->pk_params.emplace(key, p).first->second;
+    return RWKV7_OK;
+}
+
+int run_persistent(rwkv7_ctx *c, int B, bool head, bool sample) {
+    PkParams *pp = nullptr;
+    int rc = build_pk(c, B, head, &pp);
+    if (rc) return rc;
+    CK(cudaMemsetAsync(c->pkbuf, 0, c->pk_words * 4, c->stream));
+    cudaError_t e = cudaSuccess;
+    launch_persistent(*pp, c->nsm, pk_smem_bytes(pp->npad, pp->kbs, pp->stages), c->stream, &e);
+    if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "persistent step launch: %s", cudaGetErrorString(e));
+    if (head && sample) {
+        SamplerParams sp;
+        memset(&sp, 0, sizeof sp);
+        sp.B = B;
+        sp.V = c->V;
+        sp.n_slots = c->n_slots;
+        sp.slots = c->slots;
+        sp.logits = c->logits;
+        sp.occ = c->occ;
+        sp.params = c->params;
+        sp.ndraw = c->ndraw;
+        sp.lpen = c->lpen;
+        sp.next = c->next;
+        sp.err = c->errw;
+        launch_sampler(sp, LaunchCfg{c->stream, false}, &e);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "sampler launch: %s", cudaGetErrorString(e));
+    }
+    return RWKV7_OK;
+}
+
 int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
+    if (c->mode == 3) return run_persistent(c, B, head, sample);
     if (c->mode != 0) return enqueue_step(c, c->stream, B, head, sample, c->mode);
     auto key = std::make_tuple(B, (int)head, (int)sample, c->mode);
     auto it = c->graphs.find(key);
@@ -704,6 +931,14 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
         (rc = dalloc(c, &c->phg, SR * c->rg)))
         return bad(rc);
     if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
+    {
+        const int tl = 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) + row_tiles(c, L_V1) +
+                       row_tiles(c, L_G1) + row_tiles(c, L_FK);
+        c->pk_tcnt_layer = tl;
+        c->pk_words = (size_t)L * PK_NPH + 2 + (size_t)L * tl + row_tiles(c, W_HEAD) + (c->n_slots + 31) / 32 + 1 + 8 + 4 * (size_t)c->nsm;
+        if ((rc = dalloc(c, &c->pkbuf, c->pk_words))) return bad(rc);
+        if ((rc = dalloc(c, &c->p4, (size_t)PK_S4_MAX * R * F))) return bad(rc);
+    }
     const int mk[6] = {A_XR, A_XW, A_XK, A_XV, A_XA, A_XG};
     for (int q = 0; q < 6; ++q)
         if ((rc = make_amap(c, mk[q], c->xmix[q], d))) return bad(rc);
@@ -1005,7 +1240,19 @@ int rwkv7_synchronize(rwkv7_ctx *c) {
     CK(cudaMemcpy(&w, c->errw, 4, cudaMemcpyDeviceToHost));
     if (w) {
         CK(cudaMemset(c->errw, 0, 4));
-        if (w & ERR_TIMEOUT) return fail(c, RWKV7_ETIMEOUT, "a bounded wait inside a kernel gave up (flags 0x%x)", w);
+        if (w & ERR_TIMEOUT) {
+            uint32_t dg[6] = {0, 0, 0, 0, 0, 0}, pg[4] = {0, 0, 0, 0};
+            if (c->pkbuf) {
+                const size_t off = c->pk_words - 8 - 4 * (size_t)c->nsm;
+                cudaMemcpy(dg, c->pkbuf + off, sizeof dg, cudaMemcpyDeviceToHost);
+                if (dg[1] < (uint32_t)c->nsm)
+                    cudaMemcpy(pg, c->pkbuf + off + 8 + 4 * (size_t)dg[1], sizeof pg, cudaMemcpyDeviceToHost);
+            }
+            return fail(c, RWKV7_ETIMEOUT,
+                        "a bounded wait inside a kernel gave up (flags 0x%x; persistent step: where %u cta %u "
+                        "[%u %u %u %u] progress [%08x %08x %08x %08x])",
+                        w, dg[0], dg[1], dg[2], dg[3], dg[4], dg[5], pg[0], pg[1], pg[2], pg[3]);
+        }
         return fail(c, RWKV7_EINVAL, "device-side argument error (flags 0x%x: %s%s%s%s)", w,
                     (w & ERR_SLOT) ? "slot out of range " : "", (w & ERR_TOKEN) ? "token out of range " : "",
                     (w & ERR_DUP) ? "repeated slot " : "", (w & ERR_CONFIG) ? "sampler found no token" : "");
@@ -1015,7 +1262,7 @@ int rwkv7_synchronize(rwkv7_ctx *c) {
 
 int rwkv7_set_mode(rwkv7_ctx *c, int32_t mode) {
     if (!c) return RWKV7_EINVAL;
-    if (mode < 0 || mode > 2) return fail(c, RWKV7_EINVAL, "mode must be 0, 1 or 2");
+    if (mode < 0 || mode > 3) return fail(c, RWKV7_EINVAL, "mode must be 0, 1, 2 or 3");
     c->mode = mode;
     return RWKV7_OK;
 }

@@ -16,11 +16,11 @@ LOGIT_ATOL = 2e-2
 LOGIT_COS = 0.9999
 
 
-def gpu_ctx(shape: str, n_slots: int, weights: dict | None = None, mode: int = 0):
+def gpu_ctx(shape: str, n_slots: int, weights: dict | None = None, mode: int = 0, n_layer: int | None = None):
     import recurrent_decode_gb300 as rd
-    dims = synth.Dims(shape)
+    dims = synth.Dims(shape, n_layer)
     if weights is None:
-        weights = synth.make_weights(shape)
+        weights = synth.make_weights(shape, n_layer=n_layer)
     ctx = rd.Rwkv7(dims, n_slots)
     ctx.set_weights(weights)
     ctx.set_mode(mode)
