@@ -277,10 +277,14 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                         mbar_expect_tx(&full[st], W_STAGE_BYTES + XB);
                         tma_load_3d(sW + (size_t)st * W_STAGE_BYTES, wm, &full[st], 0, 0, tb + kb, polW);
                     }  // else: the weights were requested before the dependency wait
+                    if (sseg[it.s].x3) {
+                        tma_load_3d(sX + (size_t)st * XB, xm, &full[st], 0, 0, kb, polX);
+                    } else {
 #pragma unroll
-                    for (int h = 0; h < KB_STAGE; ++h)
-                        tma_load_2d(sX + (size_t)st * XB + (size_t)h * XKB, xm, &full[st], (kb + h) * GEMM_TILE_K, 0,
-                                    polX);
+                        for (int h = 0; h < KB_STAGE; ++h)
+                            tma_load_2d(sX + (size_t)st * XB + (size_t)h * XKB, xm, &full[st], (kb + h) * GEMM_TILE_K,
+                                        0, polX);
+                    }
                     ++q;
                 }
             }

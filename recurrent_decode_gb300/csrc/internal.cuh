@@ -50,6 +50,7 @@ enum Epi : int {
 // which the consuming kernel adds in slab order.
 struct GemmSeg {
     int wmap, xmap;       // tensor-map indices (tensor-core path)
+    int x3;               // 1: xmap is the 3D (col, row, k-block) view, one copy per stage
     int tile_base;        // map tile index of (this layer, row tile 0, k-block 0)
     int rows, K, kb;      // output rows, reduction length, k-blocks of 64
     int tiles, S;         // row tiles, k-splits
@@ -148,6 +149,7 @@ constexpr int PK_S4_MAX = 4;  // k-splits of the channel-mix key projection
 
 struct PkSeg {
     int wmap, xmap;          // tensor-map indices
+    int x3;                  // 1: xmap is the 3D (col, row, k-block) view, one copy per stage
     int tiles, kb, rows, S;  // row tiles, k-blocks (padded), output rows, k-splits
     int layer_tiles;         // weight-map tiles per layer (0: one matrix for all layers)
     int item0;               // first item of this segment within its phase

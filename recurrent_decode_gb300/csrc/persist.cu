@@ -1027,9 +1027,13 @@ __device__ void producer_role(const PkParams &p, const SmemTail &t, const Ring &
                     const PkSeg &sg = t.g[gemm_of(xc.l, xc.ph)].seg[xc.s];
                     const int slot = qx % rg.ns;
                     mbar_expect_tx(&rg.full[slot], (uint32_t)p.kbs * rg.xkb);
-                    for (int h = 0; h < p.kbs; ++h)
-                        tma_load_2d(rg.x + (size_t)slot * rg.slot_x + (size_t)h * rg.xkb, &p.maps[sg.xmap], &rg.full[slot],
-                                    (xc.kb + h) * GEMM_TILE_K, 0, polX);
+                    if (sg.x3) {
+                        tma_load_3d(rg.x + (size_t)slot * rg.slot_x, &p.maps[sg.xmap], &rg.full[slot], 0, 0, xc.kb, polX);
+                    } else {
+                        for (int h = 0; h < p.kbs; ++h)
+                            tma_load_2d(rg.x + (size_t)slot * rg.slot_x + (size_t)h * rg.xkb, &p.maps[sg.xmap],
+                                        &rg.full[slot], (xc.kb + h) * GEMM_TILE_K, 0, polX);
+                    }
                     cur_next(xc, p, t, c, G);
                     ++qx;
                     prog = true;

@@ -119,6 +119,8 @@ struct rwkv7_ctx {
     bool has_wmap[W_COUNT]{};
     CUtensorMap amap[A_COUNT][MAX_B / 16]{};
     bool amap_ok[A_COUNT][MAX_B / 16]{};
+    CUtensorMap amap3[A_COUNT][MAX_B / 16]{};  // (col, row, k-block) view: two k-blocks per copy
+    bool amap3_ok[A_COUNT][MAX_B / 16]{};
     void *abase[A_COUNT]{};
     int acols[A_COUNT]{};
 
@@ -217,7 +219,8 @@ int make_wmap(rwkv7_ctx *c, int kind) {
 // Split factor of a launch whose segments hold `tiles` row tiles in all:
 // enough k-splits that every SM gets about one item.
 int split_for(const rwkv7_ctx *c, int tiles) {
-    int s = c->nsm / std::max(1, tiles);
+    const int per_sm = std::max(1, std::min(4, env_int("RWKV7_GEMM_CTAS_PER_SM", 1)));
+    int s = c->nsm * per_sm / std::max(1, tiles);
     return std::max(1, std::min(s, MAX_SPLIT));
 }
 
@@ -228,6 +231,24 @@ int make_amap(rwkv7_ctx *c, int which, void *base, int cols) {
     c->acols[which] = cols;
     return RWKV7_OK;
 }
+// Activation map as a 3D view {64 cols, bcap rows, K/64 k-blocks} (row stride
+// K * 2 bytes, k-block stride 128 bytes), box {64, npad, 2}: one copy brings the
+// two k-blocks of a pipeline stage in the same shared-memory layout as two 2D
+// boxes.  Only for K a multiple of 128, so that no box reaches past a row.
+const CUtensorMap *get_amap3(rwkv7_ctx *c, int which, int npad) {
+    if (c->acols[which] % 128 != 0) return nullptr;
+    CUtensorMap &m = c->amap3[which][npad / 16 - 1];
+    if (!c->amap3_ok[which][npad / 16 - 1]) {
+        const uint64_t K = (uint64_t)c->acols[which];
+        uint64_t dims[3] = {64, (uint64_t)c->bcap, K / 64};
+        uint64_t strides[2] = {K * 2, 128};
+        uint32_t box[3] = {64, (uint32_t)npad, 2};
+        if (make_map(c, &m, c->abase[which], 3, dims, strides, box) != RWKV7_OK) return nullptr;
+        c->amap3_ok[which][npad / 16 - 1] = true;
+    }
+    return &m;
+}
+
 const CUtensorMap *get_amap(rwkv7_ctx *c, int which, int npad) {
     CUtensorMap &m = c->amap[which][npad / 16 - 1];
     if (!c->amap_ok[which][npad / 16 - 1]) {
@@ -259,6 +280,7 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
     memset(&p, 0, sizeof p);
     int nmaps = 0;
     int wslot[W_COUNT], aslot[A_COUNT];
+    bool x3slot[A_COUNT] = {};
     for (int i = 0; i < W_COUNT; ++i) wslot[i] = -1;
     for (int i = 0; i < A_COUNT; ++i) aslot[i] = -1;
     int item = 0, blk = 0;
@@ -275,13 +297,17 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         }
         if (aslot[sg.xbuf] < 0) {
             if (nmaps >= GEMM_MAX_MAPS) return fail(c, RWKV7_ECUDA, "too many tensor maps in one GEMM");
-            const CUtensorMap *am = get_amap(c, sg.xbuf, (B + 15) / 16 * 16);
+            const int np16 = (B + 15) / 16 * 16;
+            const CUtensorMap *am3 = get_amap3(c, sg.xbuf, np16);
+            const CUtensorMap *am = am3 ? am3 : get_amap(c, sg.xbuf, np16);
             if (!am) return RWKV7_ECUDA;
             aslot[sg.xbuf] = nmaps;
+            x3slot[sg.xbuf] = am3 != nullptr;
             p.maps[nmaps++] = *am;
         }
         g.wmap = wslot[sg.wkind];
         g.xmap = aslot[sg.xbuf];
+        g.x3 = x3slot[sg.xbuf] ? 1 : 0;
         g.rows = rows;
         g.K = sg.K;
         g.kb = kblocks(c, sg.wkind);
@@ -595,12 +621,15 @@ int build_pk(rwkv7_ctx *c, int B, bool head, PkParams **out) {
         }
         return wslot[kind];
     };
+    bool x3of[A_COUNT] = {};
     auto amap_of = [&](int which) -> int {
         if (aslot[which] < 0) {
             if (nmaps >= PK_MAX_MAPS) return -1;
-            const CUtensorMap *am = get_amap(c, which, p.npad);
+            const CUtensorMap *am3 = p.kbs == 2 ? get_amap3(c, which, p.npad) : nullptr;
+            const CUtensorMap *am = am3 ? am3 : get_amap(c, which, p.npad);
             if (!am) return -1;
             aslot[which] = nmaps;
+            x3of[which] = am3 != nullptr;
             p.maps[nmaps++] = *am;
         }
         return aslot[which];
@@ -621,6 +650,7 @@ int build_pk(rwkv7_ctx *c, int B, bool head, PkParams **out) {
         sg.wmap = wmap_of(kind);
         sg.xmap = amap_of(abuf);
         if (sg.wmap < 0 || sg.xmap < 0) bad_map = true;
+        sg.x3 = (sg.xmap >= 0 && x3of[abuf]) ? 1 : 0;
         sg.tiles = row_tiles(c, kind);
         sg.kb = kblocks(c, kind);
         sg.rows = c->wrows[kind];
