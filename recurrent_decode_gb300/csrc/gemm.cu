@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     __shared__ GemmSeg sseg[GEMM_MAX_SEG];
     __shared__ uint32_t snz[MAX_NZ_BLOCKS];
     __shared__ uint64_t flags_ready;
+    __shared__ uint32_t s_ok;
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int S = p.stages, B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, nitems = p.nitems;
     const bool has_skip = p.nz_skip != nullptr;
@@ -364,11 +365,20 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             bool valid = false;
             for (int kb = it.kb0; kb < it.kb1; kb += KB_STAGE)
                 if (!stage_skipped(skip, kb)) valid = true;
-            if (!mbar_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u, abort_flag)) {
-                *abort_flag = 1u;
-                atomicOr(p.err, ERR_TIMEOUT);
+            // thread 0 waits and tells the others, so that all 128 threads take
+            // the same path through the named barriers below
+            if (et == 0) s_ok = mbar_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u, abort_flag) ? 1u : 0u;
+            named_bar(3, 128);
+            const bool ok_wait = s_ok != 0u;
+            named_bar(3, 128);
+            if (!ok_wait) {
+                if (et == 0) {
+                    *abort_flag = 1u;
+                    atomicOr(p.err, ERR_TIMEOUT);
+                }
                 break;
             }
+            (void)mbar_try_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u);
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
             const int nrow = it.tile * GEMM_TILE_M + row;
