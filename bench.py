@@ -32,7 +32,12 @@ FALLBACK_HBM_GBS = 6800.0
 
 # dram bytes per launch from ncu captures, valid only while the kernel source is
 # unchanged: kernel -> (source file, sha256 prefix of it at capture, workload, bytes)
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("gemm_tc_kernel", "2.9b"): ("recurrent_decode_gb300/csrc/gemm.cu", "0ca02f0270f35209",
+                                  "2.9B shape, B=64: DRAM read+write of the 11 GEMM launches of one step of "
+                                  "a 2-layer cut (profiles/gemm_traffic_2.9b_b64.md), scaled to 32 layers + head, "
+                                  "per launch", 35820807),
+}
 
 
 def _peaks():
@@ -305,7 +310,7 @@ def main():
     dom = max(kern, key=lambda k: kern[k][0])
     dms, dn, dbytes = kern[dom]
     achieved = (dbytes / dn) / ((dms / dn) / 1e3) / 1e9
-    tr = NCU_TRAFFIC.get((dom, wl["shape"]))
+    tr = NCU_TRAFFIC.get((dom, wl["shape"])) if not args.layers else None
     traffic = None
     if tr is not None:
         src, sha, _, nbytes = tr
