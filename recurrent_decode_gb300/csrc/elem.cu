@@ -208,17 +208,34 @@ __global__ void ln_out_kernel(const ElemParams p) {
 static int ln_threads(int d) { return ((d / 8) + 31) / 32 * 32; }
 
 // ---------------------------------------------------------------------------
-// WKV7: one CTA per (head h, slot row b), 256 threads.  Thread t holds state
-// rows i0 + 16q (q = 0..3, i0 = t / 16) at columns 4(t % 16) .. +3, so every
-// 16-lane group owns whole rows and the row reductions are 4 shuffles.
+// WKV7: one CTA per (head h, slot row b), 128 threads.  The pair's 16 KB fp32
+// state lands in shared memory through one bulk copy issued before the
+// dependency wait (only this kernel, one step earlier, writes it), so registers
+// stay few and up to 12 CTAs -- 192 KB of state reads -- are in flight per SM.
 //   kh = normalize(k * k_k), kp = k * (1 + (a - 1) * k_a),
 //   vp = v (layer 0, also stored as v_first) or v + (v_first - v) * vg,
 //   S[i][j] <- S[i][j] dec_j - (sum_m S[i][m] kh_m) kh_j a_j + vp_i kp_j,
 //   y_i = sum_j S[i][j] r_j,
 //   z = (GroupNorm(y) * gamma + beta + (sum_j r_j kp_j r_k_j) vp) * g  -> fp16.
-// The state tile (16 KB) is fetched before the dependency wait: only this
-// kernel (one layer, one step earlier) writes it.
+// Thread t updates rows t/16 + 8q (q < 8) at columns 4(t % 16)..+3: the 16
+// lanes of a half-warp own a whole row (row reductions are 4 shuffles) and
+// write it back as one contiguous 256-byte segment with streaming stores.
 // ---------------------------------------------------------------------------
+constexpr int WKV_THREADS = 128;
+struct WkvSmem {
+    float st[HS * HS];
+    alignas(16) float kh[HS];
+    alignas(16) float ka[HS];
+    alignas(16) float dec[HS];
+    alignas(16) float kp[HS];
+    alignas(16) float vp[HS];
+    alignas(16) float r[HS];
+    alignas(16) float y[HS];
+    float red[4];
+    uint64_t full;
+    uint32_t ok;
+};
+
 __device__ __forceinline__ float sum64(float v, float *s2, int barid) {
     v = warp_sum(v);
     if ((threadIdx.x & 31) == 0) s2[threadIdx.x >> 5] = v;
@@ -228,39 +245,39 @@ __device__ __forceinline__ float sum64(float v, float *s2, int barid) {
     return t;
 }
 
-__global__ void __launch_bounds__(256) wkv_kernel(const WkvParams p) {
-    __shared__ __align__(16) float s_kh[HS], s_ka[HS], s_dec[HS], s_kp[HS], s_vp[HS], s_r[HS], s_y[HS];
-    __shared__ float s_red[4];
+__global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p) {
+    extern __shared__ __align__(128) uint8_t wkv_raw[];
+    WkvSmem &sm = *reinterpret_cast<WkvSmem *>(wkv_raw);
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int slot = p.slots[b];
     const bool ok = slot >= 0 && slot < p.n_slots;
     float *S = p.wkv + ((size_t)(ok ? slot : 0) * p.H + h) * (HS * HS);
-    const int i0 = tid >> 4, cg = tid & 15;
-    float4 st[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        st[q] = ok ? __ldcs((const float4 *)(S + (i0 + 16 * q) * HS + cg * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0) {
+        sm.ok = 0u;
+        mbar_init(&sm.full, 1);
+        fence_barrier_init();
+        mbar_expect_tx(&sm.full, HS * HS * 4);
+        bulk_g2s(sm.st, S, HS * HS * 4, &sm.full);
+    }
     pdl_wait();
     pdl_launch();
 
     const size_t off = (size_t)b * p.d + (size_t)h * HS;
-    float kk = 0.f, kv = 0.f, av = 0.f, vv = 0.f;
+    float rv = 0.f, kpv = 0.f, vpv = 0.f;
     if (tid < HS) {
         const int c = h * HS + tid;
-        float rv = 0.f;
+        float kv = 0.f, vv = 0.f;
         for (int j = 0; j < p.nsplit; ++j) {  // add the projection's k-split slabs in order
             const size_t o = (size_t)j * p.split_stride + off + tid;
             rv += p.r[o];
             kv += p.k[o];
             vv += p.v[o];
         }
-        av = p.a[off + tid];
-        kk = kv * __half2float(p.k_k[c]);
-        const float ss = sum64(kk * kk, s_red, 1);
-        const float nrm = fmaxf(sqrtf(ss), 1e-12f);
-        const float khv = kk / nrm;
-        const float kpv = kv * (1.0f + (av - 1.0f) * __half2float(p.k_a[c]));
-        float vpv;
+        const float av = p.a[off + tid];
+        const float kk = kv * __half2float(p.k_k[c]);
+        const float ss = sum64(kk * kk, sm.red, 1);
+        const float khv = kk / fmaxf(sqrtf(ss), 1e-12f);
+        kpv = kv * (1.0f + (av - 1.0f) * __half2float(p.k_a[c]));
         if (p.layer == 0) {
             vpv = vv;
             p.v_first[off + tid] = vv;
@@ -268,29 +285,37 @@ __global__ void __launch_bounds__(256) wkv_kernel(const WkvParams p) {
             const float vf = p.v_first[off + tid];
             vpv = vv + (vf - vv) * p.vg[off + tid];
         }
-        s_kh[tid] = khv;
-        s_ka[tid] = khv * av;
-        s_dec[tid] = p.dec[off + tid];
-        s_kp[tid] = kpv;
-        s_vp[tid] = vpv;
-        s_r[tid] = rv;
+        sm.kh[tid] = khv;
+        sm.ka[tid] = khv * av;
+        sm.dec[tid] = p.dec[off + tid];
+        sm.kp[tid] = kpv;
+        sm.vp[tid] = vpv;
+        sm.r[tid] = rv;
     }
+    if (tid == 0) sm.ok = mbar_wait(&sm.full, 0u, &sm.ok) ? 1u : 0u;  // sm.ok is 0 while waiting
     __syncthreads();
-    const float4 kh = *(const float4 *)&s_kh[cg * 4];
-    const float4 ka = *(const float4 *)&s_ka[cg * 4];
-    const float4 dc = *(const float4 *)&s_dec[cg * 4];
-    const float4 kp = *(const float4 *)&s_kp[cg * 4];
-    const float4 rr = *(const float4 *)&s_r[cg * 4];
+    const bool got = sm.ok != 0u;
+    if (!got) {  // the state copy never arrived: report; nothing is written
+        if (tid == 0) atomicOr(p.err, ERR_TIMEOUT);
+        return;
+    }
+    (void)mbar_try_wait(&sm.full, 0u);
+    const int rg = tid >> 4, cg = tid & 15;
+    const float4 kh = *(const float4 *)&sm.kh[cg * 4];
+    const float4 ka = *(const float4 *)&sm.ka[cg * 4];
+    const float4 dc = *(const float4 *)&sm.dec[cg * 4];
+    const float4 kp = *(const float4 *)&sm.kp[cg * 4];
+    const float4 rr = *(const float4 *)&sm.r[cg * 4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int i = i0 + 16 * q;
-        float4 s = st[q];
+    for (int q = 0; q < 8; ++q) {
+        const int i = rg + 8 * q;
+        float4 s = ok ? *(const float4 *)&sm.st[i * HS + cg * 4] : make_float4(0.f, 0.f, 0.f, 0.f);
         float sa = s.x * kh.x + s.y * kh.y + s.z * kh.z + s.w * kh.w;
         sa += __shfl_xor_sync(0xffffffffu, sa, 8);
         sa += __shfl_xor_sync(0xffffffffu, sa, 4);
         sa += __shfl_xor_sync(0xffffffffu, sa, 2);
         sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-        const float vpi = s_vp[i];
+        const float vpi = sm.vp[i];
         s.x = s.x * dc.x - sa * ka.x + vpi * kp.x;
         s.y = s.y * dc.y - sa * ka.y + vpi * kp.y;
         s.z = s.z * dc.z - sa * ka.z + vpi * kp.z;
@@ -300,20 +325,19 @@ __global__ void __launch_bounds__(256) wkv_kernel(const WkvParams p) {
         y += __shfl_xor_sync(0xffffffffu, y, 4);
         y += __shfl_xor_sync(0xffffffffu, y, 2);
         y += __shfl_xor_sync(0xffffffffu, y, 1);
-        if (cg == 0) s_y[i] = y;
+        if (cg == 0) sm.y[i] = y;
         if (ok) __stcs((float4 *)(S + i * HS + cg * 4), s);
     }
     __syncthreads();
     if (tid < HS) {
         const int c = h * HS + tid;
-        const float yv = s_y[tid];
-        const float mean = sum64(yv, s_red, 1) * (1.0f / HS);
+        const float yv = sm.y[tid];
+        const float mean = sum64(yv, sm.red, 1) * (1.0f / HS);
         const float dv = yv - mean;
-        const float var = sum64(dv * dv, s_red, 1) * (1.0f / HS);
+        const float var = sum64(dv * dv, sm.red, 1) * (1.0f / HS);
         const float yn = dv * (1.0f / sqrtf(var + 64e-5f)) * __half2float(p.lnx_w[c]) + __half2float(p.lnx_b[c]);
-        const float bonus = sum64(s_r[tid] * s_kp[tid] * __half2float(p.r_k[c]), s_red, 1);
-        const float zv = (yn + bonus * s_vp[tid]) * p.g[off + tid];
-        p.z[off + tid] = __float2half_rn(zv);
+        const float bonus = sum64(rv * kpv * __half2float(p.r_k[c]), sm.red, 1);
+        p.z[off + tid] = __float2half_rn((yn + bonus * vpv) * p.g[off + tid]);
     }
 }
 
@@ -433,8 +457,18 @@ void launch_ln_out(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e) {
 }
 
 void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e) {
+    static bool attr_set = false;
+    const size_t smem = sizeof(WkvSmem);
+    if (!attr_set) {
+        cudaError_t r = cudaFuncSetAttribute(wkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (r != cudaSuccess) {
+            *e = r;
+            return;
+        }
+        attr_set = true;
+    }
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = mkcfg(dim3(p.H, p.B), dim3(256), 0, lc, at);
+    cudaLaunchConfig_t cfg = mkcfg(dim3(p.H, p.B), dim3(WKV_THREADS), smem, lc, at);
     cudaError_t r = cudaLaunchKernelEx(&cfg, wkv_kernel, p);
     if (r != cudaSuccess) *e = r;
 }
