@@ -192,6 +192,67 @@ def _config(wl, dm, args):
             "l2": "inputs larger than L2 (weights + states per step >> 126 MB), no flush"}
 
 
+def secondary(config, steps, args, dev, world):
+    """The same timed decode loop on another named workload (graph replay,
+    CUDA events, clocks sampled): throughput and whole-step roofline."""
+    import torch
+    import recurrent_decode_gb300 as rd
+    wl = synth.WORKLOADS[config]
+    dm = synth.Dims(wl["shape"])
+    B = wl["B"]
+    weights = synth.make_weights(wl["shape"])
+    ctx = rd.Rwkv7(dm, B)
+    ctx.set_weights(weights)
+    del weights
+    if args.mode >= 0:
+        ctx.set_mode(args.mode)
+    for s in range(B):
+        if wl.get("greedy"):
+            ctx.set_sampling(s, greedy=True)
+        else:
+            ctx.set_sampling(s, temperature=wl["temperature"], top_p=wl["top_p"], top_k=wl["top_k"],
+                             presence=wl["presence"], frequency=wl["frequency"],
+                             penalty_decay=wl["penalty_decay"], seed=synth.SAMPLING_SEED_BASE + s)
+    slots = torch.arange(B, dtype=torch.int32, device=dev)
+    prompts = torch.from_numpy(synth.prompt_tokens(dm.vocab, B, wl["prompt"])).to(dev)
+    for t in range(wl["prompt"] - 1):
+        ctx.decode_step(slots, prompts[:, t].contiguous())
+    tokens = prompts[:, -1].contiguous()
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        ctx.decode_step(slots, tokens, None, nxt)
+        tokens.copy_(nxt)
+    ctx.synchronize()
+    dev_id = None
+    try:
+        dev_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    clk = ClockSampler(dev_id)
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        ctx.decode_step(slots, tokens, None, nxt)
+        tokens.copy_(nxt)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1)
+    ctx.synchronize()
+    ctx.close()
+    peak, peak_kind = _peaks()
+    sb = step_bytes(dm, B)
+    gbs = sb / (ms / steps / 1e3) / 1e9
+    return {"config": _config(wl, dm, argparse.Namespace(steps=steps)), "value": world * B * steps / (ms / 1e3),
+            "unit": "tok/s", "steps": steps, "ms_per_step": ms / steps,
+            "step_roofline": {"bytes_per_step": sb, "achieved_GBps": gbs, "frac_of_peak": gbs / peak,
+                              "peak_kind": peak_kind, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS},
+            "clocks": clocks}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -205,6 +266,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run a model with this many layers of the shape's sizes")
     ap.add_argument("--prompt", type=int, default=0, help="profiling only: override the prompt length")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the 7.2B-shape measurement added to the 2.9B line")
     ap.add_argument("--mode", type=int, default=-1,
                     help="implementation: 0 multi-kernel CUDA graph, 3 persistent kernel (default: library default)")
     args = ap.parse_args()
@@ -333,11 +396,14 @@ def main():
         "gpu_launches": ctx.step_kernel_count(B, True) * args.steps,
         "clocks": clocks,
     }
+    ctx.close()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(weights, dm, wl, args.cpu_seconds)
+    if args.config == "2.9b" and world == 1 and not args.layers and not args.prompt and not args.no_secondary:
+        # the metric names both shapes: the 7.2B workload rides along on the same line
+        line["secondary"] = secondary("7.2b", max(16, min(64, args.steps)), args, dev, world)
     if rank == 0:
         print(json.dumps(line))
-    ctx.close()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
