@@ -108,7 +108,7 @@ __global__ void embed_kernel(const ElemParams p) {
     const int b = blockIdx.x;
     const int i0 = threadIdx.x * 8;
     const bool act = i0 < p.d;
-    const int slot = p.slots[b];
+    const int slot = p.single_slot >= 0 ? p.single_slot : p.slots[b];
     int tok = p.tokens[b];
     if (threadIdx.x == 0) {
         if (slot < 0 || slot >= p.n_slots) atomicOr(p.err, ERR_SLOT);
@@ -124,7 +124,7 @@ __global__ void embed_kernel(const ElemParams p) {
     }
     ln8(v, act, p.d, w4, b4, red);
     if (act) st8f(p.x + (size_t)b * p.d + i0, v);
-    if (b == 0) {
+    if (b == 0 && p.single_slot < 0) {
         const int words = (p.n_slots + 31) / 32;
         for (int i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
         __syncthreads();
@@ -341,6 +341,191 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill LayerNorm + token shift: CTA t normalises token t and, for the shift,
+// token t-1 again (row 0 takes the slot's shift state), so no CTA waits for
+// another.  x is read only; the residual with the slabs added goes to xout.
+// CTA 0 also normalises the last token and stores it as the new shift state,
+// after it has read the old one.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ln_row(const ElemParams &p, int t, int i0, bool act, const uint4 &w4, const uint4 &b4,
+                                       float (&v)[8], float *red) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+    if (act) {
+        ld8f(p.x + (size_t)t * p.d + i0, v);
+        if (p.part) add_slabs(v, p.part, p.nsplit, p.split_stride, (size_t)t * p.d + i0);
+    }
+    ln8(v, act, p.d, w4, b4, red);
+}
+
+template <int NMIX>
+__global__ void ln_mix_prefill_kernel(const ElemParams p) {
+    __shared__ float red[32];
+    const int t = blockIdx.x, n = gridDim.x;
+    const int i0 = threadIdx.x * 8;
+    const bool act = i0 < p.d;
+    const int slot = p.single_slot;
+    const bool ok = slot >= 0 && slot < p.n_slots;
+    uint4 w4 = make_uint4(0, 0, 0, 0), b4 = w4, mu4[NMIX];
+    float sh[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float *shp = p.shift + (size_t)(ok ? slot : 0) * p.d + i0;
+    if (act) {
+        w4 = *reinterpret_cast<const uint4 *>(p.ln_w + i0);
+        b4 = *reinterpret_cast<const uint4 *>(p.ln_b + i0);
+#pragma unroll
+        for (int q = 0; q < NMIX; ++q) mu4[q] = *reinterpret_cast<const uint4 *>(p.mu[q] + i0);
+        if (t == 0 && ok) ld8f(shp, sh);
+    }
+    pdl_wait();
+    pdl_launch();
+    float v[8];
+    if (act) {  // residual of this token for the next phase
+        float xv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xv[k] = 0.0f;
+        ld8f(p.x + (size_t)t * p.d + i0, xv);
+        if (p.part) add_slabs(xv, p.part, p.nsplit, p.split_stride, (size_t)t * p.d + i0);
+        st8f(p.xout + (size_t)t * p.d + i0, xv);
+    }
+    ln_row(p, t, i0, act, w4, b4, v, red);
+    if (t > 0) ln_row(p, t - 1, i0, act, w4, b4, sh, red);
+    if (t == 0 && n > 1) {
+        float last[8];
+        ln_row(p, n - 1, i0, act, w4, b4, last, red);
+        __syncthreads();  // every thread has read the old shift state
+        if (act && ok) st8f(shp, last);
+    } else if (t == 0) {
+        __syncthreads();
+        if (act && ok) st8f(shp, v);
+    }
+    if (!act) return;
+#pragma unroll
+    for (int q = 0; q < NMIX; ++q) {
+        float mu[8], o[8];
+        h8_to_f(mu4[q], mu);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = v[k] + (sh[k] - v[k]) * mu[k];
+        *reinterpret_cast<uint4 *>(p.xo[q] + (size_t)t * p.d + i0) = f_to_h8(o);
+    }
+}
+
+// Per (token t, head h), 64 threads (channel j): the WKV vectors.
+__global__ void __launch_bounds__(64) wkv_vec_kernel(const WkvSeqParams p) {
+    __shared__ float red[2];
+    const int h = blockIdx.x, t = blockIdx.y, j = threadIdx.x;
+    pdl_wait();
+    pdl_launch();
+    const int c = h * HS + j;
+    const size_t off = (size_t)t * p.d + c;
+    float rv = 0.f, kv = 0.f, vv = 0.f;
+    for (int s = 0; s < p.nsplit; ++s) {
+        const size_t o = (size_t)s * p.split_stride + off;
+        rv += p.r[o];
+        kv += p.k[o];
+        vv += p.v[o];
+    }
+    const float av = p.a[off];
+    const float kk = kv * __half2float(p.k_k[c]);
+    const float ss = sum64(kk * kk, red, 1);
+    const float khv = kk / fmaxf(sqrtf(ss), 1e-12f);
+    const float kpv = kv * (1.0f + (av - 1.0f) * __half2float(p.k_a[c]));
+    float vpv;
+    if (p.layer == 0) {
+        vpv = vv;
+        p.v_first[off] = vv;
+    } else {
+        vpv = vv + (p.v_first[off] - vv) * p.vg[off];
+    }
+    const float bonus = sum64(rv * kpv * __half2float(p.r_k[c]), red, 1);
+    p.kh[off] = khv;
+    p.ka[off] = khv * av;
+    p.kp[off] = kpv;
+    p.vp[off] = vpv;
+    p.rr[off] = rv;
+    if (j == 0) p.bonus[(size_t)t * p.H + h] = bonus;
+}
+
+// The sequential update of one slot's state over n tokens.  CTA (h, part)
+// owns state rows 16*part .. +16 of head h (rows are independent given the
+// vectors); thread t: row 16*part + t/8, columns 8*(t%8) .. +8, so the 8
+// threads of a row reduce with 3 shuffles.  The vectors of 32 tokens at a time
+// are staged in shared memory.
+constexpr int WSQ_TB = 32;
+__global__ void __launch_bounds__(128) wkv_seq_kernel(const WkvSeqParams p) {
+    __shared__ __align__(16) float vec[WSQ_TB][6][HS];  // kh, ka, dec, kp, r, vp
+    const int h = blockIdx.x, part = blockIdx.y, tid = threadIdx.x;
+    const int i = 16 * part + (tid >> 3), cb = 8 * (tid & 7);
+    const bool ok = p.slot >= 0 && p.slot < p.n_slots;
+    float *S = p.wkv + ((size_t)(ok ? p.slot : 0) * p.H + h) * (HS * HS) + (size_t)i * HS + cb;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    if (ok) {
+        s0 = *(const float4 *)S;
+        s1 = *(const float4 *)(S + 4);
+    }
+    pdl_wait();
+    pdl_launch();
+    for (int t0 = 0; t0 < p.n; t0 += WSQ_TB) {
+        const int nb = min(WSQ_TB, p.n - t0);
+        __syncthreads();
+        for (int e = tid; e < nb * 6 * HS; e += 128) {
+            const int tt = e / (6 * HS), r = e - tt * 6 * HS, which = r / HS, col = r - which * HS;
+            const size_t off = (size_t)(t0 + tt) * p.d + (size_t)h * HS + col;
+            const float *src = which == 0 ? p.kh : which == 1 ? p.ka : which == 2 ? p.dec : which == 3 ? p.kp
+                                                                         : which == 4 ? p.rr : p.vp;
+            vec[tt][which][col] = src[off];
+        }
+        __syncthreads();
+        for (int tt = 0; tt < nb; ++tt) {
+            const float4 kh0 = *(const float4 *)&vec[tt][0][cb], kh1 = *(const float4 *)&vec[tt][0][cb + 4];
+            float sa = s0.x * kh0.x + s0.y * kh0.y + s0.z * kh0.z + s0.w * kh0.w + s1.x * kh1.x + s1.y * kh1.y +
+                       s1.z * kh1.z + s1.w * kh1.w;
+            sa += __shfl_xor_sync(0xffffffffu, sa, 4);
+            sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+            sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+            const float4 ka0 = *(const float4 *)&vec[tt][1][cb], ka1 = *(const float4 *)&vec[tt][1][cb + 4];
+            const float4 dc0 = *(const float4 *)&vec[tt][2][cb], dc1 = *(const float4 *)&vec[tt][2][cb + 4];
+            const float4 kp0 = *(const float4 *)&vec[tt][3][cb], kp1 = *(const float4 *)&vec[tt][3][cb + 4];
+            const float4 r0 = *(const float4 *)&vec[tt][4][cb], r1 = *(const float4 *)&vec[tt][4][cb + 4];
+            const float vpi = vec[tt][5][i];
+            s0.x = s0.x * dc0.x - sa * ka0.x + vpi * kp0.x;
+            s0.y = s0.y * dc0.y - sa * ka0.y + vpi * kp0.y;
+            s0.z = s0.z * dc0.z - sa * ka0.z + vpi * kp0.z;
+            s0.w = s0.w * dc0.w - sa * ka0.w + vpi * kp0.w;
+            s1.x = s1.x * dc1.x - sa * ka1.x + vpi * kp1.x;
+            s1.y = s1.y * dc1.y - sa * ka1.y + vpi * kp1.y;
+            s1.z = s1.z * dc1.z - sa * ka1.z + vpi * kp1.z;
+            s1.w = s1.w * dc1.w - sa * ka1.w + vpi * kp1.w;
+            float y = s0.x * r0.x + s0.y * r0.y + s0.z * r0.z + s0.w * r0.w + s1.x * r1.x + s1.y * r1.y +
+                      s1.z * r1.z + s1.w * r1.w;
+            y += __shfl_xor_sync(0xffffffffu, y, 4);
+            y += __shfl_xor_sync(0xffffffffu, y, 2);
+            y += __shfl_xor_sync(0xffffffffu, y, 1);
+            if ((tid & 7) == 0) p.y[(size_t)(t0 + tt) * p.d + (size_t)h * HS + i] = y;
+        }
+    }
+    if (ok) {
+        *(float4 *)S = s0;
+        *(float4 *)(S + 4) = s1;
+    }
+}
+
+// Per (token t, head h), 64 threads: z = (GroupNorm(y) * gamma + beta + bonus * vp) * g.
+__global__ void __launch_bounds__(64) wkv_gate_kernel(const WkvSeqParams p) {
+    __shared__ float red[2];
+    const int h = blockIdx.x, t = blockIdx.y, j = threadIdx.x;
+    pdl_wait();
+    pdl_launch();
+    const int c = h * HS + j;
+    const size_t off = (size_t)t * p.d + c;
+    const float yv = p.y[off];
+    const float mean = sum64(yv, red, 1) * (1.0f / HS);
+    const float dv = yv - mean;
+    const float var = sum64(dv * dv, red, 1) * (1.0f / HS);
+    const float yn = dv * (1.0f / sqrtf(var + 64e-5f)) * __half2float(p.lnx_w[c]) + __half2float(p.lnx_b[c]);
+    p.z[off] = __float2half_rn((yn + p.bonus[(size_t)t * p.H + h] * p.vp[off]) * p.g[off]);
+}
+
 // LoRA-down outputs: one CTA per slot row; column c of LoRA i is the sum of the
 // S partial slabs, passed through the LoRA's activation and rounded to fp16.
 __global__ void lora_fin_kernel(const LoraFinParams p) {
@@ -446,6 +631,29 @@ void launch_ln_mix(const ElemParams &p, int nmix, const LaunchCfg &lc, cudaError
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(ln_threads(p.d)), 0, lc, at);
     cudaError_t r = nmix == 6 ? cudaLaunchKernelEx(&cfg, ln_mix_kernel<6>, p) : cudaLaunchKernelEx(&cfg, ln_mix_kernel<1>, p);
+    if (r != cudaSuccess) *e = r;
+}
+
+void launch_ln_mix_prefill(const ElemParams &p, int nmix, const LaunchCfg &lc, cudaError_t *e) {
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(ln_threads(p.d)), 0, lc, at);
+    cudaError_t r = nmix == 6 ? cudaLaunchKernelEx(&cfg, ln_mix_prefill_kernel<6>, p)
+                              : cudaLaunchKernelEx(&cfg, ln_mix_prefill_kernel<1>, p);
+    if (r != cudaSuccess) *e = r;
+}
+
+void launch_wkv_prefill(const WkvSeqParams &p, const LaunchCfg &lc, cudaError_t *e) {
+    cudaLaunchAttribute at[1];
+    cudaLaunchConfig_t c1 = mkcfg(dim3(p.H, p.n), dim3(64), 0, lc, at);
+    cudaError_t r = cudaLaunchKernelEx(&c1, wkv_vec_kernel, p);
+    if (r == cudaSuccess) {
+        cudaLaunchConfig_t c2 = mkcfg(dim3(p.H, 4), dim3(128), 0, lc, at);
+        r = cudaLaunchKernelEx(&c2, wkv_seq_kernel, p);
+    }
+    if (r == cudaSuccess) {
+        cudaLaunchConfig_t c3 = mkcfg(dim3(p.H, p.n), dim3(64), 0, lc, at);
+        r = cudaLaunchKernelEx(&c3, wkv_gate_kernel, p);
+    }
     if (r != cudaSuccess) *e = r;
 }
 

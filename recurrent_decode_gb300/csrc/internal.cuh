@@ -103,9 +103,34 @@ struct ElemParams {
     int nsplit;
     long long split_stride;
     uint32_t *err;
+    int single_slot;          // prefill: every row is a token of this slot (-1: rows are slots)
+    float *xout;              // prefill: residual after the slab adds (x is read only)
 };
 
 void launch_embed(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
+// Prefill of one slot: rows are the consecutive tokens of a chunk.  The token
+// shift takes the previous row's LayerNorm output (the slot's shift state for
+// row 0) and leaves the last row's in the shift state.
+void launch_ln_mix_prefill(const ElemParams &p, int nmix, const LaunchCfg &lc, cudaError_t *e);
+
+// Prefill WKV of one slot over n tokens, in three kernels:
+//  vectors per (token, head): kh, kh*a, kp, vp, r and the bonus scalar;
+//  the sequential state update (4 CTAs per head, 16 state rows each): y;
+//  GroupNorm + bonus + output gate: z.
+struct WkvSeqParams {
+    int n, d, H, slot, n_slots, layer;
+    const float *r, *k, *v;          // projection split slabs [nsplit][bcap][d]
+    int nsplit;
+    long long split_stride;
+    const float *dec, *a, *vg, *g;   // [n][d]
+    float *v_first;                  // [n][d]
+    const __half *k_k, *k_a, *r_k, *lnx_w, *lnx_b;
+    float *kh, *ka, *kp, *vp, *rr, *bonus, *y;  // prefill work buffers [n][d] ([n][H] bonus)
+    float *wkv;                      // this layer's states [n_slots][H][64][64]
+    __half *z;                       // [n][d]
+    uint32_t *err;
+};
+void launch_wkv_prefill(const WkvSeqParams &p, const LaunchCfg &lc, cudaError_t *e);
 void launch_ln_mix(const ElemParams &p, int nmix, const LaunchCfg &lc, cudaError_t *e);
 void launch_ln_out(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
 

@@ -113,6 +113,9 @@ struct rwkv7_ctx {
     float *pr = nullptr, *pk = nullptr, *pv = nullptr, *phw = nullptr, *pha = nullptr, *phv = nullptr,
           *phg = nullptr, *px = nullptr;
     uint32_t *errw = nullptr;
+    // prefill: second residual buffer and WKV work buffers [bcap][d] ([bcap][H] bonus)
+    float *x2 = nullptr, *pf_kh = nullptr, *pf_ka = nullptr, *pf_kp = nullptr, *pf_vp = nullptr, *pf_r = nullptr,
+          *pf_y = nullptr, *pf_bonus = nullptr;
 
     CUtensorMap wmap[W_COUNT]{};
     CUtensorMap wmap1[W_COUNT]{};  // box of one k-block tile (persistent step with N > 128)
@@ -387,6 +390,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     const int d = c->d;
     ElemParams ep;
     memset(&ep, 0, sizeof ep);
+    ep.single_slot = -1;
     ep.B = B;
     ep.d = d;
     ep.H = c->H;
@@ -793,6 +797,164 @@ int run_persistent(rwkv7_ctx *c, int B, bool head, bool sample) {
     return RWKV7_OK;
 }
 
+// ---------------------------------------------------------------- chunked prefill
+// n consecutive tokens of one slot (tokens in c->tokens): the tokens form the
+// N side of every projection, so each weight is streamed once per chunk.
+int enqueue_prefill(rwkv7_ctx *c, cudaStream_t st, int slot, int n, bool head) {
+    const int mode = c->mode == 3 ? 0 : c->mode;
+    LaunchCfg lc{st, mode != 2};
+    LaunchCfg lc0{st, false};
+    cudaError_t e = cudaSuccess;
+    const int d = c->d;
+    ElemParams ep;
+    memset(&ep, 0, sizeof ep);
+    ep.B = n;
+    ep.d = d;
+    ep.H = c->H;
+    ep.F = c->F;
+    ep.V = c->V;
+    ep.n_slots = c->n_slots;
+    ep.L = c->L;
+    ep.slots = c->slots;
+    ep.tokens = c->tokens;
+    ep.x = c->x;
+    ep.err = c->errw;
+    ep.single_slot = slot;
+    ep.emb = c->w[W_EMB];
+    ep.ln_w = c->w[W_LN0W];
+    ep.ln_b = c->w[W_LN0B];
+    launch_embed(ep, lc0, &e);
+    if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "embed launch: %s", cudaGetErrorString(e));
+    int rc;
+    const int s1 = std::min(split_for(c, 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) +
+                                             row_tiles(c, L_V1) + row_tiles(c, L_G1)),
+                            kblocks(c, L_WR) / 2);
+    const int s3 = std::min(split_for(c, row_tiles(c, L_WO)), kblocks(c, L_WO) / 2);
+    const int s5 = std::min(split_for(c, row_tiles(c, L_FV)), kblocks(c, L_FV) / 2);
+    const long long xstride = (long long)c->bcap * d;
+    float *xa = c->x, *xb = c->x2;  // residual in, residual out of each LayerNorm phase
+    int px_splits = 0;
+    for (int l = 0; l < c->L; ++l) {
+        ElemParams m = ep;
+        m.layer = l;
+        m.x = xa;
+        m.xout = xb;
+        m.ln_w = LW(c, L_LN1W, l);
+        m.ln_b = LW(c, L_LN1B, l);
+        const int mk[6] = {L_XR, L_XW, L_XK, L_XV, L_XA, L_XG};
+        for (int q = 0; q < 6; ++q) {
+            m.mu[q] = LW(c, mk[q], l);
+            m.xo[q] = c->xmix[q];
+        }
+        m.shift = c->shift_att + (size_t)l * c->n_slots * d;
+        m.part = px_splits ? c->px : nullptr;
+        m.nsplit = px_splits;
+        m.split_stride = xstride;
+        launch_ln_mix_prefill(m, 6, lc, &e);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
+        Seg g1[7];
+        int n1 = 0;
+        g1[n1++] = {L_WR, A_XR, c->xmix[0], d, EPI_F32, c->pr, d, nullptr, s1};
+        g1[n1++] = {L_WK, A_XK, c->xmix[2], d, EPI_F32, c->pk, d, nullptr, s1};
+        g1[n1++] = {L_WV, A_XV, c->xmix[3], d, EPI_F32, c->pv, d, nullptr, s1};
+        g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F32, c->phw, c->rw, nullptr, s1};
+        g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F32, c->pha, c->ra, nullptr, s1};
+        if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F32, c->phv, c->rv, nullptr, s1};
+        g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, s1};
+        if ((rc = run_gemm(c, l, g1, n1, n, nullptr, nullptr, lc, mode))) return rc;
+        LoraFinParams lf;
+        memset(&lf, 0, sizeof lf);
+        lf.B = n;
+        lf.S = s1;
+        lf.r[0] = c->rw; lf.r[1] = c->ra; lf.r[2] = l > 0 ? c->rv : 0; lf.r[3] = c->rg;
+        lf.part[0] = c->phw; lf.part[1] = c->pha; lf.part[2] = c->phv; lf.part[3] = c->phg;
+        lf.out[0] = c->hw; lf.out[1] = c->ha; lf.out[2] = c->hv; lf.out[3] = c->hg;
+        lf.act[0] = 1; lf.act[1] = 0; lf.act[2] = 0; lf.act[3] = 2;
+        lf.bcap = c->bcap;
+        launch_lora_fin(lf, lc, &e);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "lora_fin launch: %s", cudaGetErrorString(e));
+        Seg g2[4];
+        int n2 = 0;
+        g2[n2++] = {L_W2, A_HW, c->hw, c->rw, EPI_DECAY, c->dec, d, LW(c, L_W0, l), 1};
+        g2[n2++] = {L_A2, A_HA, c->ha, c->ra, EPI_SIGMOID_BIAS, c->a, d, LW(c, L_A0, l), 1};
+        if (l > 0) g2[n2++] = {L_V2, A_HV, c->hv, c->rv, EPI_SIGMOID_BIAS, c->vg, d, LW(c, L_V0, l), 1};
+        g2[n2++] = {L_G2, A_HG, c->hg, c->rg, EPI_F32, c->g, d, nullptr, 1};
+        if ((rc = run_gemm(c, l, g2, n2, n, nullptr, nullptr, lc, mode))) return rc;
+        WkvSeqParams wp;
+        memset(&wp, 0, sizeof wp);
+        wp.n = n;
+        wp.d = d;
+        wp.H = c->H;
+        wp.slot = slot;
+        wp.n_slots = c->n_slots;
+        wp.layer = l;
+        wp.r = c->pr;
+        wp.k = c->pk;
+        wp.v = c->pv;
+        wp.nsplit = s1;
+        wp.split_stride = xstride;
+        wp.dec = c->dec;
+        wp.a = c->a;
+        wp.vg = c->vg;
+        wp.g = c->g;
+        wp.v_first = c->vfirst;
+        wp.k_k = LW(c, L_KK, l);
+        wp.k_a = LW(c, L_KA, l);
+        wp.r_k = LW(c, L_RK, l);
+        wp.lnx_w = LW(c, L_LNXW, l);
+        wp.lnx_b = LW(c, L_LNXB, l);
+        wp.kh = c->pf_kh;
+        wp.ka = c->pf_ka;
+        wp.kp = c->pf_kp;
+        wp.vp = c->pf_vp;
+        wp.rr = c->pf_r;
+        wp.bonus = c->pf_bonus;
+        wp.y = c->pf_y;
+        wp.wkv = c->wkv + (size_t)l * c->n_slots * c->H * HS * HS;
+        wp.z = c->z;
+        wp.err = c->errw;
+        launch_wkv_prefill(wp, lc, &e);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "wkv prefill launch: %s", cudaGetErrorString(e));
+        Seg g3[1] = {{L_WO, A_Z, c->z, d, EPI_F32, c->px, d, nullptr, s3}};
+        if ((rc = run_gemm(c, l, g3, 1, n, nullptr, nullptr, lc, mode))) return rc;
+        ElemParams m2 = ep;
+        m2.layer = l;
+        m2.x = xb;
+        m2.xout = xa;
+        m2.ln_w = LW(c, L_LN2W, l);
+        m2.ln_b = LW(c, L_LN2B, l);
+        m2.mu[0] = LW(c, L_FXK, l);
+        m2.xo[0] = c->xk;
+        m2.shift = c->shift_ffn + (size_t)l * c->n_slots * d;
+        m2.part = c->px;
+        m2.nsplit = s3;
+        m2.split_stride = xstride;
+        launch_ln_mix_prefill(m2, 1, lc, &e);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
+        Seg g4[1] = {{L_FK, A_XKF, c->xk, d, EPI_RELU2, c->h, c->F, nullptr, 1}};
+        if ((rc = run_gemm(c, l, g4, 1, n, c->nz, nullptr, lc, mode))) return rc;
+        Seg g5[1] = {{L_FV, A_H, c->h, c->F, EPI_F32, c->px, d, nullptr, s5}};
+        if ((rc = run_gemm(c, l, g5, 1, n, nullptr, c->nz, lc, mode))) return rc;
+        px_splits = s5;
+    }
+    if (head) {  // logits of the last token only
+        ElemParams o = ep;
+        o.B = 1;
+        o.x = xa + (size_t)(n - 1) * d;
+        o.ln_w = c->w[W_LNOW];
+        o.ln_b = c->w[W_LNOB];
+        o.xo[0] = c->xo;
+        o.part = c->px + (size_t)(n - 1) * d;
+        o.nsplit = px_splits;
+        o.split_stride = xstride;
+        launch_ln_out(o, lc, &e);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_out launch: %s", cudaGetErrorString(e));
+        Seg gh[1] = {{W_HEAD, A_XO, c->xo, d, EPI_F32, c->logits, c->V, nullptr, 1}};
+        if ((rc = run_gemm(c, 0, gh, 1, 1, nullptr, nullptr, lc, mode))) return rc;
+    }
+    return RWKV7_OK;
+}
+
 int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
     if (c->mode == 3) return run_persistent(c, B, head, sample);
     if (c->mode != 0) return enqueue_step(c, c->stream, B, head, sample, c->mode);
@@ -819,7 +981,6 @@ int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
     return RWKV7_OK;
 }
 
-__global__ void set_i32_kernel(int32_t *p, int32_t v) { *p = v; }
 
 int check_ready(rwkv7_ctx *c) {
     if (c->n_missing) return fail(c, RWKV7_ESTATE, "%zu weight tensors have not been set", c->n_missing);
@@ -879,7 +1040,8 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
     c->rv = g.lora_v;
     c->rg = g.lora_g;
     c->n_slots = g.n_slots;
-    c->bcap = (std::min(g.n_slots, MAX_B) + 15) / 16 * 16;
+    // activation rows: a fused decode step of up to 256 slots, or a prefill chunk of 256 tokens
+    c->bcap = MAX_B;
     c->stream = (cudaStream_t)cuda_stream;
     int dev = 0;
     int rc = RWKV7_OK;
@@ -961,6 +1123,10 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
         (rc = dalloc(c, &c->phg, SR * c->rg)))
         return bad(rc);
     if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
+    if ((rc = dalloc(c, &c->x2, R * d)) || (rc = dalloc(c, &c->pf_kh, R * d)) || (rc = dalloc(c, &c->pf_ka, R * d)) ||
+        (rc = dalloc(c, &c->pf_kp, R * d)) || (rc = dalloc(c, &c->pf_vp, R * d)) || (rc = dalloc(c, &c->pf_r, R * d)) ||
+        (rc = dalloc(c, &c->pf_y, R * d)) || (rc = dalloc(c, &c->pf_bonus, R * c->H)))
+        return bad(rc);
     {
         const int tl = 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) + row_tiles(c, L_V1) +
                        row_tiles(c, L_G1) + row_tiles(c, L_FK);
@@ -1173,12 +1339,12 @@ int rwkv7_prefill_seq(rwkv7_ctx *c, int32_t slot, const int32_t *d_tokens, int32
     if (!SLOT_OK(slot) || !d_tokens || T <= 0) return fail(c, RWKV7_EINVAL, "bad slot, token pointer or length");
     int rc;
     if ((rc = check_ready(c))) return rc;
-    set_i32_kernel<<<1, 1, 0, c->stream>>>(c->slots, slot);
-    CK(cudaGetLastError());
-    for (int t = 0; t < T; ++t) {
-        CK(cudaMemcpyAsync(c->tokens, d_tokens + t, 4, cudaMemcpyDeviceToDevice, c->stream));
-        const bool last = (t == T - 1) && d_logits_out;
-        if ((rc = run_step(c, 1, last, false))) return rc;
+    // chunks of up to bcap tokens; every weight is streamed once per chunk
+    for (int s0 = 0; s0 < T; s0 += c->bcap) {
+        const int n = std::min(c->bcap, T - s0);
+        CK(cudaMemcpyAsync(c->tokens, d_tokens + s0, (size_t)n * 4, cudaMemcpyDeviceToDevice, c->stream));
+        const bool last = (s0 + n == T) && d_logits_out;
+        if ((rc = enqueue_prefill(c, c->stream, slot, n, last))) return rc;
     }
     if (d_logits_out)
         CK(cudaMemcpyAsync(d_logits_out, c->logits, (size_t)c->V * 4, cudaMemcpyDeviceToDevice, c->stream));
