@@ -358,6 +358,25 @@ def main():
     e2e_s = time.perf_counter() - t0
     e2e_val = world * B * args.e2e_steps / e2e_s
 
+    # prefill throughput: one slot consumes a 1024-token prompt (4 chunks of 256)
+    pre = None
+    if not args.layers and not args.prompt:
+        ptoks = torch.from_numpy(synth.prompt_tokens(dm.vocab, 1, 1024, seed=7)[0]).to(dev)
+        plog = torch.empty(dm.vocab, device=dev)
+        ctx.prefill_seq(0, ptoks, plog)  # warm-up
+        ctx.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        ctx.prefill_seq(0, ptoks, plog)
+        p1.record(stream)
+        ctx.synchronize()
+        pms = p0.elapsed_time(p1)
+        body = synth.n_params(dm) - 2 * dm.vocab * dm.d_model  # all but the embedding and the head
+        flops = 2.0 * body * 1024 + 2.0 * dm.vocab * dm.d_model
+        pre = {"tokens": 1024, "ms": pms, "tok_per_s": 1024 / (pms / 1e3), "tflops": flops / (pms / 1e3) / 1e12,
+               "note": "one slot, 4 chunks of 256 tokens; FLOPs = 2 x non-embedding, non-head parameters x tokens "
+                       "+ the head for the last token"}
+
     # per-kernel-class device time of one directly launched step (events)
     prof = ctx.profile_step(slots, tokens, with_sampling=True)
     cb = class_bytes(dm, B)
@@ -394,6 +413,7 @@ def main():
         "e2e": {"value": e2e_val, "unit": "tok/s", "h2d_bytes_per_step": 2 * B * 4, "d2h_bytes_per_step": B * 4,
                 "steps": args.e2e_steps},
         "gpu_launches": ctx.step_kernel_count(B, True) * args.steps,
+        "prefill": pre,
         "clocks": clocks,
     }
     ctx.close()
