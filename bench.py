@@ -187,9 +187,67 @@ def run_reference(args, wl, dm):
 def _config(wl, dm, args):
     return {"workload": f"RWKV-7 {dm.name} shape batched greedy decode" if wl.get("greedy")
             else f"RWKV-7 {dm.name} shape batched sampled decode (top_p {wl.get('top_p')})",
-            "shape": dm.name, "n_layer": dm.n_layer, "B": wl["B"], "prompt_tokens": wl["prompt"], "decode_steps_timed": args.steps,
+            "shape": dm.name, "n_layer": dm.n_layer, "B": wl.get("B", wl.get("n_slots")),
+            "prompt_tokens": wl.get("prompt", wl.get("prompt_range")), "decode_steps_timed": args.steps,
             "weights": "random-init fp16 (seed 0)", "state": "fp32",
             "l2": "inputs larger than L2 (weights + states per step >> 126 MB), no flush"}
+
+
+def run_trace_bench(args, wl):
+    """The continuous-batching trace: every request to completion through the
+    worker loop (recurrent_decode_gb300.trace); value = generated tokens per
+    second of wall time, prefills included."""
+    import torch
+    import recurrent_decode_gb300 as rd
+    from recurrent_decode_gb300.trace import Request, run_trace
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dm = synth.Dims(wl["shape"])
+    weights = synth.make_weights(wl["shape"])
+    ctx = rd.Rwkv7(dm, wl["n_slots"])
+    ctx.set_weights(weights)
+    del weights
+    if args.mode >= 0:
+        ctx.set_mode(args.mode)
+    lens = synth.trace_requests(wl["n_req"], *wl["prompt_range"], *wl["out_range"])
+    reqs = []
+    for i, (pl, ol) in enumerate(lens):
+        sp = dict(temperature=wl["temperature"], top_p=wl["top_p"], top_k=wl["top_k"], presence=wl["presence"],
+                  frequency=wl["frequency"], penalty_decay=wl["penalty_decay"],
+                  seed=synth.SAMPLING_SEED_BASE + i, greedy=False)
+        reqs.append(Request(prompt=synth.prompt_tokens(dm.vocab, 1, pl, seed=10000 + i)[0], n_out=ol, sampling=sp))
+    dev_id = None
+    try:
+        dev_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    torch.cuda.synchronize()
+    clk = ClockSampler(dev_id)
+    stats = run_trace(ctx, reqs, wl["n_slots"], decode_prefill_ratio=wl["decode_prefill_ratio"],
+                      min_forward_seq_len=wl["min_forward_seq_len"])
+    clocks = clk.stop()
+    ctx.close()
+    ttft = np.array(stats.ttft_s)
+    total_in = stats.prefill_tokens + stats.decode_fed_tokens + stats.generated
+    line = {"metric": METRIC, "value": world * stats.generated / stats.wall_s, "unit": "tok/s", "n_gpus": world,
+            "steps": stats.rounds, "warmup": 0, "ms_per_step": stats.wall_s * 1e3 / max(1, stats.rounds),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": {"workload": f"continuous-batching trace on the {dm.name} shape ({args.config})",
+                       "shape": dm.name, "slots": wl["n_slots"], "requests": wl["n_req"],
+                       "prompt_range": list(wl["prompt_range"]), "output_range": list(wl["out_range"]),
+                       "decode_prefill_ratio": wl["decode_prefill_ratio"],
+                       "weights": "random-init fp16 (seed 0)"},
+            "trace": {"generated_tokens": stats.generated, "prefill_tokens": stats.prefill_tokens,
+                      "decode_fed_tokens": stats.decode_fed_tokens, "rounds": stats.rounds,
+                      "wall_s": stats.wall_s, "prefill_share": stats.prefill_tokens / max(1, total_in),
+                      "ttft_s_p50": float(np.percentile(ttft, 50)), "ttft_s_p90": float(np.percentile(ttft, 90))},
+            "clocks": clocks}
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
 
 
 def secondary(config, steps, args, dev, world):
@@ -273,6 +331,8 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = dict(synth.WORKLOADS[args.config])
+    if args.config.startswith("trace") and args.impl != "reference":
+        return run_trace_bench(args, wl)
     if args.prompt:
         wl["prompt"] = max(2, args.prompt)
     dm = synth.Dims(wl["shape"], args.layers or None)

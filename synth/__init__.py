@@ -45,6 +45,15 @@ WORKLOADS = {
     "7.2b": dict(shape="7.2b", B=256, prompt=64, steps=256, greedy=False,
                  temperature=1.0, top_p=0.3, top_k=0, presence=0.0, frequency=1.0,
                  penalty_decay=0.996),
+    # continuous-batching traces: 256 requests through 128 slots, one prefill phase
+    # per 5 decode rounds; prompts as written (U[20, 2000]) or as the pages'
+    # measured mix (~3 % prefill tokens: U[20, 138])
+    "trace": dict(shape="2.9b", n_slots=128, n_req=256, prompt_range=(20, 2000), out_range=(1000, 3000),
+                  decode_prefill_ratio=5, min_forward_seq_len=10, temperature=1.0, top_p=0.3, top_k=0,
+                  presence=0.0, frequency=1.0, penalty_decay=0.996),
+    "trace-3pct": dict(shape="2.9b", n_slots=128, n_req=256, prompt_range=(20, 138), out_range=(1000, 3000),
+                       decode_prefill_ratio=5, min_forward_seq_len=10, temperature=1.0, top_p=0.3, top_k=0,
+                       presence=0.0, frequency=1.0, penalty_decay=0.996),
 }
 
 WEIGHT_SEED = 0
