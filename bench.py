@@ -387,6 +387,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    ctx.ffn_union_stats()  # reset: count the timed steps only
     clk = ClockSampler(dev_id)
     time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -403,6 +404,7 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     value = world * B * args.steps / (ms / 1e3)
+    nzb, totb = ctx.ffn_union_stats()
 
     # end to end through the host-buffer entry point (pinned host memory)
     h_slots = torch.arange(B, dtype=torch.int32).pin_memory()
@@ -474,6 +476,9 @@ def main():
                 "steps": args.e2e_steps},
         "gpu_launches": ctx.step_kernel_count(B, True) * args.steps,
         "prefill": pre,
+        "ffn_union": {"nonzero_blocks": nzb, "blocks": totb, "fraction": nzb / max(1, totb),
+                      "note": "64-row blocks of the channel-mix value matrix read by the sparse value projection "
+                              "over the timed steps; the roofline counts the dense bytes"},
         "clocks": clocks,
     }
     ctx.close()

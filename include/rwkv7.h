@@ -200,6 +200,16 @@ RWKV7_API int rwkv7_set_mode(rwkv7_ctx *ctx, int32_t mode);
 RWKV7_API int rwkv7_get_io_buffers(rwkv7_ctx *ctx, int32_t **d_slots, int32_t **d_tokens, float **d_logits,
                          int32_t **d_next);
 
+/* Sparse channel mix (RWKV-Server article, "RWKV 批量推理中 Prefill 的正确打开方式"
+ * §三: cmix_sparse_one / cmix_sparse_rows skip the value rows whose ReLU^2
+ * input is zero): the value projection reads only the 64-row blocks of the
+ * value matrix whose hidden block is nonzero for some slot of the step.  This
+ * returns, since the previous call (or rwkv7_create), the number of such
+ * nonzero blocks and the number of blocks considered (layers x d_ffn/64 per
+ * step or prefill chunk; the persistent mode computes the value projection
+ * densely and is not counted), then resets both.  Synchronous. */
+RWKV7_API int rwkv7_ffn_union_stats(rwkv7_ctx *ctx, uint64_t *nonzero_blocks, uint64_t *blocks);
+
 /* Kernel classes of rwkv7_profile_step, in output order. */
 #define RWKV7_PROF_EMBED 0       /* embedding + LayerNorm 0 (+ slot/token checks) */
 #define RWKV7_PROF_LN_MIX 1      /* LayerNorm + token-shift mixes (time and channel mix) */

@@ -61,6 +61,7 @@ SIGNATURES = {
     "rwkv7_sample_rows_static": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                            C.POINTER(C.c_char_p)]),
+    "rwkv7_ffn_union_stats": (C.c_int, [_VP, C.POINTER(C.c_uint64), C.POINTER(C.c_uint64)]),
     "rwkv7_synchronize": (C.c_int, [_VP]),
     "rwkv7_set_mode": (C.c_int, [_VP, C.c_int32]),
     "rwkv7_get_io_buffers": (C.c_int, [_VP, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
@@ -263,6 +264,13 @@ class Rwkv7:
         self._check(self.lib.rwkv7_sample_batch(self.h, _ptr(slots, torch.int32, "slots"),
                                                 _ptr(logits, torch.float32, "logits"), slots.numel(),
                                                 _ptr(next_out, torch.int32, "next_out")))
+
+    def ffn_union_stats(self):
+        """(nonzero value-row blocks, blocks considered) since the last call; see
+        rwkv7_ffn_union_stats."""
+        nz, tot = C.c_uint64(), C.c_uint64()
+        self._check(self.lib.rwkv7_ffn_union_stats(self.h, C.byref(nz), C.byref(tot)))
+        return int(nz.value), int(tot.value)
 
     def synchronize(self):
         self._check(self.lib.rwkv7_synchronize(self.h))

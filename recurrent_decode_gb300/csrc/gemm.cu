@@ -392,8 +392,11 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                 if (et == 0) {
                     const int blk0 = it.tile * 2;
                     const int nblk = (sg.rows + 63) / 64;
-                    if (blk0 < nblk) nz_out[blk0] = nzq[0] | nzq[1];
-                    if (blk0 + 1 < nblk) nz_out[blk0 + 1] = nzq[2] | nzq[3];
+                    const uint32_t f0 = nzq[0] | nzq[1], f1 = nzq[2] | nzq[3];
+                    if (blk0 < nblk) nz_out[blk0] = f0;
+                    if (blk0 + 1 < nblk) nz_out[blk0 + 1] = f1;
+                    const unsigned long long nnz = (blk0 < nblk ? f0 : 0u) + (blk0 + 1 < nblk ? f1 : 0u);
+                    if (p.nz_count && nnz) atomicAdd(p.nz_count, nnz);
                 }
                 named_bar(2, 128);
             }
@@ -513,6 +516,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
             uint32_t f = 0;
             for (int w = 0; w < 8; ++w) f |= nzw[w];
             p.nz_out[blk] = f;
+            if (p.nz_count && f) atomicAdd(p.nz_count, 1ull);
         }
     }
 }

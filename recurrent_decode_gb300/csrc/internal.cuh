@@ -74,6 +74,7 @@ struct GemmParams {
     int accbufs;                     // TMEM accumulator buffers (1 or 2)
     int prefetch;                    // 1: weights may be fetched before the dependency wait
     uint32_t *nz_out;                // EPI_RELU2: flag per 64 output rows
+    unsigned long long *nz_count;    // EPI_RELU2: running count of nonzero 64-row blocks (or null)
     const uint32_t *nz_skip;         // nonzero flags per k-block of the activations (or null)
     uint32_t *err;
 };

@@ -113,6 +113,8 @@ struct rwkv7_ctx {
     float *pr = nullptr, *pk = nullptr, *pv = nullptr, *phw = nullptr, *pha = nullptr, *phv = nullptr,
           *phg = nullptr, *px = nullptr;
     uint32_t *errw = nullptr;
+    unsigned long long *nzstat = nullptr;  // nonzero channel-mix blocks counted by the key projection
+    unsigned long long nz_considered = 0;  // blocks those counts cover (host side)
     // prefill: second residual buffer and WKV work buffers [bcap][d] ([bcap][H] bonus)
     float *x2 = nullptr, *pf_kh = nullptr, *pf_ka = nullptr, *pf_kp = nullptr, *pf_vp = nullptr, *pf_r = nullptr,
           *pf_y = nullptr, *pf_bonus = nullptr;
@@ -281,6 +283,7 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
              const LaunchCfg &lc, int mode) {
     GemmParams p;
     memset(&p, 0, sizeof p);
+    p.nz_count = nz_out ? c->nzstat : nullptr;
     int nmaps = 0;
     int wslot[W_COUNT], aslot[A_COUNT];
     bool x3slot[A_COUNT] = {};
@@ -957,6 +960,7 @@ int enqueue_prefill(rwkv7_ctx *c, cudaStream_t st, int slot, int n, bool head) {
 
 int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
     if (c->mode == 3) return run_persistent(c, B, head, sample);
+    c->nz_considered += (unsigned long long)c->L * ((c->F + 63) / 64);
     if (c->mode != 0) return enqueue_step(c, c->stream, B, head, sample, c->mode);
     auto key = std::make_tuple(B, (int)head, (int)sample, c->mode);
     auto it = c->graphs.find(key);
@@ -1123,6 +1127,7 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
         (rc = dalloc(c, &c->phg, SR * c->rg)))
         return bad(rc);
     if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
+    if ((rc = dalloc(c, &c->nzstat, 4))) return bad(rc);
     if ((rc = dalloc(c, &c->x2, R * d)) || (rc = dalloc(c, &c->pf_kh, R * d)) || (rc = dalloc(c, &c->pf_ka, R * d)) ||
         (rc = dalloc(c, &c->pf_kp, R * d)) || (rc = dalloc(c, &c->pf_vp, R * d)) || (rc = dalloc(c, &c->pf_r, R * d)) ||
         (rc = dalloc(c, &c->pf_y, R * d)) || (rc = dalloc(c, &c->pf_bonus, R * c->H)))
@@ -1345,6 +1350,7 @@ int rwkv7_prefill_seq(rwkv7_ctx *c, int32_t slot, const int32_t *d_tokens, int32
         CK(cudaMemcpyAsync(c->tokens, d_tokens + s0, (size_t)n * 4, cudaMemcpyDeviceToDevice, c->stream));
         const bool last = (s0 + n == T) && d_logits_out;
         if ((rc = enqueue_prefill(c, c->stream, slot, n, last))) return rc;
+        c->nz_considered += (unsigned long long)c->L * ((c->F + 63) / 64);
     }
     if (d_logits_out)
         CK(cudaMemcpyAsync(d_logits_out, c->logits, (size_t)c->V * 4, cudaMemcpyDeviceToDevice, c->stream));
@@ -1469,6 +1475,19 @@ int32_t rwkv7_step_kernel_count(const rwkv7_ctx *c, int32_t B, int32_t with_samp
     return sub * (1 + 9 * c->L + 2 + (with_sampling ? 1 : 0));
 }
 
+int rwkv7_ffn_union_stats(rwkv7_ctx *c, uint64_t *nonzero_blocks, uint64_t *blocks) {
+    if (!c) return RWKV7_EINVAL;
+    if (!nonzero_blocks || !blocks) return fail(c, RWKV7_EINVAL, "null argument");
+    CK(cudaStreamSynchronize(c->stream));
+    unsigned long long nz = 0;
+    CK(cudaMemcpy(&nz, c->nzstat, sizeof nz, cudaMemcpyDeviceToHost));
+    CK(cudaMemset(c->nzstat, 0, sizeof nz));
+    *nonzero_blocks = nz;
+    *blocks = c->nz_considered;
+    c->nz_considered = 0;
+    return RWKV7_OK;
+}
+
 int rwkv7_profile_step(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_tokens, int32_t B,
                        int32_t with_sampling, float *ms_out, int32_t *launches_out, int32_t n_classes) {
     if (!c) return RWKV7_EINVAL;
@@ -1483,6 +1502,7 @@ int rwkv7_profile_step(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_to
     pf.n = 0;
     pf.cls.clear();
     const int mode = c->mode == 2 ? 2 : 1;
+    c->nz_considered += (unsigned long long)c->L * ((c->F + 63) / 64);
     if ((rc = enqueue_step(c, c->stream, B, true, with_sampling != 0, mode, &pf))) return rc;
     CK(cudaStreamSynchronize(c->stream));
     for (int i = 0; i < n_classes; ++i) {

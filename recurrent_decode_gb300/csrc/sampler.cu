@@ -245,9 +245,15 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     // ---- pass B: weight sums per (q1 >> 12) bucket
     for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
     __syncthreads();
+    // At temperature 1 the draw weights are the q1 weights, so they are
+    // computed once here and stored over the row's penalised logits; the later
+    // passes read them back.  Otherwise every pass recomputes them from lp.
+    const bool t1 = sp.temperature == 1.0f;
+    uint32_t *lq = reinterpret_cast<uint32_t *>(lp);
     unsigned long long q1loc = 0;
     for (int i = tid; i < V; i += SMP_THREADS) {
         const uint32_t q = qweight(lp[i], m, 1.0f);
+        if (t1) lq[i] = q;
         q1loc += q;
         if (q) atomicAdd(&sm.hist[q >> 12], (unsigned long long)q);
     }
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
     __syncthreads();
     for (int i = tid; i < V; i += SMP_THREADS) {
-        const uint32_t q = qweight(lp[i], m, 1.0f);
+        const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
         if ((int)(q >> 12) == hb && q) atomicAdd(&sm.hist[q & 4095u], (unsigned long long)q);
     }
     __syncthreads();
@@ -277,14 +283,14 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
         const unsigned long long K = (unsigned long long)sp.top_k;
         for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
         __syncthreads();
-        for (int i = tid; i < V; i += SMP_THREADS) atomicAdd(&sm.hist[qweight(lp[i], m, 1.0f) >> 12], 1ull);
+        for (int i = tid; i < V; i += SMP_THREADS) atomicAdd(&sm.hist[(t1 ? lq[i] : qweight(lp[i], m, 1.0f)) >> 12], 1ull);
         __syncthreads();
         unsigned long long cabove;
         const int hk = find_cut(sm, NBUCKET, 0ull, K, &cabove);
         for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
         __syncthreads();
         for (int i = tid; i < V; i += SMP_THREADS) {
-            const uint32_t q = qweight(lp[i], m, 1.0f);
+            const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
             if ((int)(q >> 12) == hk) atomicAdd(&sm.hist[q & 4095u], 1ull);
         }
         __syncthreads();
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     unsigned long long tie_base = 0;
     if (use_k) {
         unsigned long long ties = 0;
-        for (int i = i_lo; i < i_hi; ++i) ties += (qweight(lp[i], m, 1.0f) == tk);
+        for (int i = i_lo; i < i_hi; ++i) ties += ((t1 ? lq[i] : qweight(lp[i], m, 1.0f)) == tk);
         unsigned long long tt;
         tie_base = block_excl_scan(ties, sm, &tt);
     }
@@ -308,14 +314,14 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     {
         unsigned long long tie_seen = tie_base;
         for (int i = i_lo; i < i_hi; ++i) {
-            const uint32_t q = qweight(lp[i], m, 1.0f);
+            const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
             bool keep = q >= tp;
             if (use_k) {
                 const bool tie = (q == tk);
                 keep = keep && (q > tk || (tie && tie_seen < need_ties));
                 tie_seen += tie;
             }
-            if (keep) rloc += (sp.temperature == 1.0f) ? q : qweight(lp[i], m, sp.temperature);
+            if (keep) rloc += t1 ? q : qweight(lp[i], m, sp.temperature);
         }
     }
     unsigned long long R;
@@ -330,7 +336,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     if (rloc > 0 && rbase <= r && r < rbase + rloc) {
         unsigned long long acc = rbase, tie_seen = tie_base;
         for (int i = i_lo; i < i_hi; ++i) {
-            const uint32_t q = qweight(lp[i], m, 1.0f);
+            const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
             bool keep = q >= tp;
             if (use_k) {
                 const bool tie = (q == tk);
@@ -338,7 +344,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
                 tie_seen += tie;
             }
             if (!keep) continue;
-            acc += (sp.temperature == 1.0f) ? q : qweight(lp[i], m, sp.temperature);
+            acc += t1 ? q : qweight(lp[i], m, sp.temperature);
             if (acc > r) {
                 sm.ibcast[1] = i;
                 break;

@@ -149,6 +149,40 @@ def test_persistent_at_2p9b_layer_sizes():
             assert_logits_close(outs[1][t][i], sts[k].step(int(toks[i])), f"oracle step {t} row {i}")
 
 
+def _zero(a):
+    a[...] = 0
+
+
+def test_sparse_value_projection():
+    """Channel-mix key weights zero: ReLU^2 input is zero everywhere, the value
+    projection skips every block (union 0 of all) and the logits still match the
+    oracle's dense channel mix; with the seeded weights nearly every block is
+    read."""
+    torch = _torch()
+    dev = torch.device("cuda")
+    dims = synth.Dims("tiny")
+    ov = {f"blocks.{l}.ffn.key": _zero for l in range(dims.n_layer)}
+    for W, expect_zero in ((synth.make_weights("tiny", overrides=ov), True), (synth.make_weights("tiny"), False)):
+        ctx, _, _ = gpu_ctx("tiny", 4, W, 0)
+        m, sts = oracle_states(W, dims, 3)
+        lg = torch.empty(3, dims.vocab, device=dev)
+        ctx.ffn_union_stats()
+        for t in range(3):
+            toks = synth.prompt_tokens(dims.vocab, 3, 1, seed=130 + t)[:, 0]
+            ctx.decode_step(torch.arange(3, dtype=torch.int32, device=dev), torch.from_numpy(toks).to(dev), lg)
+            ctx.synchronize()
+            got = lg.cpu().numpy()
+            for i in range(3):
+                assert_logits_close(got[i], sts[i].step(int(toks[i])), f"step {t} row {i}")
+        nz, tot = ctx.ffn_union_stats()
+        assert tot == 3 * dims.n_layer * (dims.d_ffn // 64)
+        if expect_zero:
+            assert nz == 0
+        else:
+            assert nz >= 0.9 * tot
+        ctx.close()
+
+
 def test_batch_invariance_bit_exact(tiny):
     """A slot's logits do not depend on B or on its position in the batch."""
     torch = _torch()
