@@ -438,22 +438,38 @@ __global__ void __launch_bounds__(64) wkv_vec_kernel(const WkvSeqParams p) {
         vpv = vv + (p.v_first[off] - vv) * p.vg[off];
     }
     const float bonus = sum64(rv * kpv * __half2float(p.r_k[c]), red, 1);
-    p.kh[off] = khv;
-    p.ka[off] = khv * av;
-    p.kp[off] = kpv;
-    p.vp[off] = vpv;
-    p.rr[off] = rv;
+    float *vec = p.vec + ((size_t)h * p.vec_rows + t) * (6 * HS) + j;
+    vec[0 * HS] = khv;
+    vec[1 * HS] = khv * av;
+    vec[2 * HS] = p.dec[off];
+    vec[3 * HS] = kpv;
+    vec[4 * HS] = rv;
+    vec[5 * HS] = vpv;
     if (j == 0) p.bonus[(size_t)t * p.H + h] = bonus;
 }
 
 // The sequential update of one slot's state over n tokens.  CTA (h, part)
 // owns state rows 16*part .. +16 of head h (rows are independent given the
 // vectors); thread t: row 16*part + t/8, columns 8*(t%8) .. +8, so the 8
-// threads of a row reduce with 3 shuffles.  The vectors of 32 tokens at a time
-// are staged in shared memory.
+// threads of a row reduce with 3 shuffles.  The vectors of a head are stored
+// per token as 6 x 64 contiguous floats, so 32 tokens are one 48 KB block: one
+// bulk copy per block, two blocks in flight.
 constexpr int WSQ_TB = 32;
+constexpr uint32_t WSQ_BLOCK = WSQ_TB * 6 * HS * 4;  // bytes
+struct WsqSmem {
+    float vec[2][WSQ_TB][6][HS];
+    uint64_t full[2];
+    uint32_t stop;
+};
+__device__ __forceinline__ void wsq_issue(const WkvSeqParams &p, WsqSmem &sm, int h, int blk) {
+    const int t0 = blk * WSQ_TB, nb = min(WSQ_TB, p.n - t0);
+    const uint32_t bytes = (uint32_t)nb * 6 * HS * 4;
+    mbar_expect_tx(&sm.full[blk & 1], bytes);
+    bulk_g2s(&sm.vec[blk & 1][0][0][0], p.vec + ((size_t)h * p.vec_rows + t0) * (6 * HS), bytes, &sm.full[blk & 1]);
+}
 __global__ void __launch_bounds__(128) wkv_seq_kernel(const WkvSeqParams p) {
-    __shared__ __align__(16) float vec[WSQ_TB][6][HS];  // kh, ka, dec, kp, r, vp
+    extern __shared__ __align__(128) uint8_t wsq_raw[];
+    WsqSmem &sm = *reinterpret_cast<WsqSmem *>(wsq_raw);
     const int h = blockIdx.x, part = blockIdx.y, tid = threadIdx.x;
     const int i = 16 * part + (tid >> 3), cb = 8 * (tid & 7);
     const bool ok = p.slot >= 0 && p.slot < p.n_slots;
@@ -463,31 +479,40 @@ __global__ void __launch_bounds__(128) wkv_seq_kernel(const WkvSeqParams p) {
         s0 = *(const float4 *)S;
         s1 = *(const float4 *)(S + 4);
     }
-    pdl_wait();
+    const int nblk = (p.n + WSQ_TB - 1) / WSQ_TB;
+    if (tid == 0) {
+        sm.stop = 0u;
+        mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.full[1], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();  // the vectors come from the preceding kernel
     pdl_launch();
-    for (int t0 = 0; t0 < p.n; t0 += WSQ_TB) {
-        const int nb = min(WSQ_TB, p.n - t0);
+    if (tid == 0)
+        for (int k = 0; k < 2 && k < nblk; ++k) wsq_issue(p, sm, h, k);
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int t0 = blk * WSQ_TB, nb = min(WSQ_TB, p.n - t0), buf = blk & 1;
+        if (tid == 0) sm.stop = mbar_wait(&sm.full[buf], (uint32_t)(blk >> 1) & 1u, &sm.stop) ? 0u : 2u;
         __syncthreads();
-        for (int e = tid; e < nb * 6 * HS; e += 128) {
-            const int tt = e / (6 * HS), r = e - tt * 6 * HS, which = r / HS, col = r - which * HS;
-            const size_t off = (size_t)(t0 + tt) * p.d + (size_t)h * HS + col;
-            const float *src = which == 0 ? p.kh : which == 1 ? p.ka : which == 2 ? p.dec : which == 3 ? p.kp
-                                                                         : which == 4 ? p.rr : p.vp;
-            vec[tt][which][col] = src[off];
+        if (sm.stop) {  // a vector block never arrived: report and leave the state as it was
+            if (tid == 0) atomicOr(p.err, ERR_TIMEOUT);
+            return;
         }
-        __syncthreads();
+        (void)mbar_try_wait(&sm.full[buf], (uint32_t)(blk >> 1) & 1u);
         for (int tt = 0; tt < nb; ++tt) {
-            const float4 kh0 = *(const float4 *)&vec[tt][0][cb], kh1 = *(const float4 *)&vec[tt][0][cb + 4];
+            const float *vv = &sm.vec[buf][tt][0][0];
+            const float4 kh0 = *(const float4 *)&vv[0 * HS + cb], kh1 = *(const float4 *)&vv[0 * HS + cb + 4];
             float sa = s0.x * kh0.x + s0.y * kh0.y + s0.z * kh0.z + s0.w * kh0.w + s1.x * kh1.x + s1.y * kh1.y +
                        s1.z * kh1.z + s1.w * kh1.w;
             sa += __shfl_xor_sync(0xffffffffu, sa, 4);
             sa += __shfl_xor_sync(0xffffffffu, sa, 2);
             sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-            const float4 ka0 = *(const float4 *)&vec[tt][1][cb], ka1 = *(const float4 *)&vec[tt][1][cb + 4];
-            const float4 dc0 = *(const float4 *)&vec[tt][2][cb], dc1 = *(const float4 *)&vec[tt][2][cb + 4];
-            const float4 kp0 = *(const float4 *)&vec[tt][3][cb], kp1 = *(const float4 *)&vec[tt][3][cb + 4];
-            const float4 r0 = *(const float4 *)&vec[tt][4][cb], r1 = *(const float4 *)&vec[tt][4][cb + 4];
-            const float vpi = vec[tt][5][i];
+            const float4 ka0 = *(const float4 *)&vv[1 * HS + cb], ka1 = *(const float4 *)&vv[1 * HS + cb + 4];
+            const float4 dc0 = *(const float4 *)&vv[2 * HS + cb], dc1 = *(const float4 *)&vv[2 * HS + cb + 4];
+            const float4 kp0 = *(const float4 *)&vv[3 * HS + cb], kp1 = *(const float4 *)&vv[3 * HS + cb + 4];
+            const float4 r0 = *(const float4 *)&vv[4 * HS + cb], r1 = *(const float4 *)&vv[4 * HS + cb + 4];
+            const float vpi = vv[5 * HS + i];
             s0.x = s0.x * dc0.x - sa * ka0.x + vpi * kp0.x;
             s0.y = s0.y * dc0.y - sa * ka0.y + vpi * kp0.y;
             s0.z = s0.z * dc0.z - sa * ka0.z + vpi * kp0.z;
@@ -503,6 +528,8 @@ __global__ void __launch_bounds__(128) wkv_seq_kernel(const WkvSeqParams p) {
             y += __shfl_xor_sync(0xffffffffu, y, 1);
             if ((tid & 7) == 0) p.y[(size_t)(t0 + tt) * p.d + (size_t)h * HS + i] = y;
         }
+        __syncthreads();  // buffer fully read
+        if (tid == 0 && blk + 2 < nblk) wsq_issue(p, sm, h, blk + 2);
     }
     if (ok) {
         *(float4 *)S = s0;
@@ -523,7 +550,8 @@ __global__ void __launch_bounds__(64) wkv_gate_kernel(const WkvSeqParams p) {
     const float dv = yv - mean;
     const float var = sum64(dv * dv, red, 1) * (1.0f / HS);
     const float yn = dv * (1.0f / sqrtf(var + 64e-5f)) * __half2float(p.lnx_w[c]) + __half2float(p.lnx_b[c]);
-    p.z[off] = __float2half_rn((yn + p.bonus[(size_t)t * p.H + h] * p.vp[off]) * p.g[off]);
+    const float vpv = p.vec[((size_t)h * p.vec_rows + t) * (6 * HS) + 5 * HS + j];
+    p.z[off] = __float2half_rn((yn + p.bonus[(size_t)t * p.H + h] * vpv) * p.g[off]);
 }
 
 // LoRA-down outputs: one CTA per slot row; column c of LoRA i is the sum of the
@@ -647,7 +675,14 @@ void launch_wkv_prefill(const WkvSeqParams &p, const LaunchCfg &lc, cudaError_t 
     cudaLaunchConfig_t c1 = mkcfg(dim3(p.H, p.n), dim3(64), 0, lc, at);
     cudaError_t r = cudaLaunchKernelEx(&c1, wkv_vec_kernel, p);
     if (r == cudaSuccess) {
-        cudaLaunchConfig_t c2 = mkcfg(dim3(p.H, 4), dim3(128), 0, lc, at);
+        static bool attr_set = false;
+        if (!attr_set) {
+            r = cudaFuncSetAttribute(wkv_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(WsqSmem));
+            attr_set = r == cudaSuccess;
+        }
+    }
+    if (r == cudaSuccess) {
+        cudaLaunchConfig_t c2 = mkcfg(dim3(p.H, 4), dim3(128), sizeof(WsqSmem), lc, at);
         r = cudaLaunchKernelEx(&c2, wkv_seq_kernel, p);
     }
     if (r == cudaSuccess) {

@@ -126,7 +126,9 @@ struct WkvSeqParams {
     const float *dec, *a, *vg, *g;   // [n][d]
     float *v_first;                  // [n][d]
     const __half *k_k, *k_a, *r_k, *lnx_w, *lnx_b;
-    float *kh, *ka, *kp, *vp, *rr, *bonus, *y;  // prefill work buffers [n][d] ([n][H] bonus)
+    float *vec;                      // per-head vectors [H][vec_rows][6][64]: kh, kh*a, dec, kp, r, vp
+    int vec_rows;
+    float *bonus, *y;                // [n][H], [n][d]
     float *wkv;                      // this layer's states [n_slots][H][64][64]
     __half *z;                       // [n][d]
     uint32_t *err;

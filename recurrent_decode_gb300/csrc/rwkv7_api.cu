@@ -116,8 +116,7 @@ struct rwkv7_ctx {
     unsigned long long *nzstat = nullptr;  // nonzero channel-mix blocks counted by the key projection
     unsigned long long nz_considered = 0;  // blocks those counts cover (host side)
     // prefill: second residual buffer and WKV work buffers [bcap][d] ([bcap][H] bonus)
-    float *x2 = nullptr, *pf_kh = nullptr, *pf_ka = nullptr, *pf_kp = nullptr, *pf_vp = nullptr, *pf_r = nullptr,
-          *pf_y = nullptr, *pf_bonus = nullptr;
+    float *x2 = nullptr, *pf_vec = nullptr, *pf_y = nullptr, *pf_bonus = nullptr;
 
     CUtensorMap wmap[W_COUNT]{};
     CUtensorMap wmap1[W_COUNT]{};  // box of one k-block tile (persistent step with N > 128)
@@ -906,11 +905,8 @@ int enqueue_prefill(rwkv7_ctx *c, cudaStream_t st, int slot, int n, bool head) {
         wp.r_k = LW(c, L_RK, l);
         wp.lnx_w = LW(c, L_LNXW, l);
         wp.lnx_b = LW(c, L_LNXB, l);
-        wp.kh = c->pf_kh;
-        wp.ka = c->pf_ka;
-        wp.kp = c->pf_kp;
-        wp.vp = c->pf_vp;
-        wp.rr = c->pf_r;
+        wp.vec = c->pf_vec;
+        wp.vec_rows = c->bcap;
         wp.bonus = c->pf_bonus;
         wp.y = c->pf_y;
         wp.wkv = c->wkv + (size_t)l * c->n_slots * c->H * HS * HS;
@@ -1128,8 +1124,7 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
         return bad(rc);
     if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
     if ((rc = dalloc(c, &c->nzstat, 4))) return bad(rc);
-    if ((rc = dalloc(c, &c->x2, R * d)) || (rc = dalloc(c, &c->pf_kh, R * d)) || (rc = dalloc(c, &c->pf_ka, R * d)) ||
-        (rc = dalloc(c, &c->pf_kp, R * d)) || (rc = dalloc(c, &c->pf_vp, R * d)) || (rc = dalloc(c, &c->pf_r, R * d)) ||
+    if ((rc = dalloc(c, &c->x2, R * d)) || (rc = dalloc(c, &c->pf_vec, R * 6 * (size_t)d)) ||
         (rc = dalloc(c, &c->pf_y, R * d)) || (rc = dalloc(c, &c->pf_bonus, R * c->H)))
         return bad(rc);
     {
