@@ -149,6 +149,40 @@ def test_persistent_at_2p9b_layer_sizes():
             assert_logits_close(outs[1][t][i], sts[k].step(int(toks[i])), f"oracle step {t} row {i}")
 
 
+def test_batch_beyond_one_fused_step(tiny):
+    """B = 300 slots (more than one fused step of 256): the step runs as two
+    sub-steps; rows from both match the oracle, and the host-buffer entry point
+    gives the device-buffer path's logits and tokens bit for bit."""
+    torch = _torch()
+    dev = torch.device("cuda")
+    B = 300
+    ctxs = []
+    for _ in range(2):
+        ctx, W, dims = gpu_ctx("tiny", B, tiny, 0)
+        for s in range(B):
+            ctx.set_sampling(s, greedy=True)
+        ctxs.append(ctx)
+    slots = np.random.default_rng(17).permutation(B).astype(np.int32)
+    rows = [0, 131, 255, 256, 299]
+    m, sts = oracle_states(tiny, dims, len(rows))
+    lg = torch.empty(B, dims.vocab, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    h_lg = np.zeros((B, dims.vocab), np.float32)
+    h_nx = np.zeros(B, np.int32)
+    toks = synth.prompt_tokens(dims.vocab, B, 1, seed=140)[:, 0]
+    for step in range(2):
+        ctxs[0].decode_step(torch.from_numpy(slots).to(dev), torch.from_numpy(toks).to(dev), lg, nxt)
+        ctxs[0].synchronize()
+        ctxs[1].decode_step_host(slots, toks, h_lg, h_nx)
+        got = lg.cpu().numpy()
+        assert np.array_equal(got, h_lg) and np.array_equal(nxt.cpu().numpy(), h_nx)
+        for k, i in enumerate(rows):
+            assert_logits_close(got[i], sts[k].step(int(toks[i])), f"step {step} row {i}")
+        toks = nxt.cpu().numpy().copy()
+    for ctx in ctxs:
+        ctx.close()
+
+
 def _zero(a):
     a[...] = 0
 
