@@ -28,6 +28,10 @@ namespace rk {
 
 constexpr int SMP_THREADS = 1024;
 constexpr int NBUCKET = 4097;  // q1 >> 12 for q1 in [0, 2^24]
+// Elements per thread per step of a pass over the row: independent loads issued
+// together, so that a pass is not bound by one load's latency at a time.
+constexpr int SMP_U = 8;
+constexpr int SMP_STEP = SMP_U * SMP_THREADS;
 
 // 2^e for e <= 0: e = n + f (n nearest integer, f exact), 2^f by its degree-7
 // Taylor polynomial in f ln 2 (coefficients (ln 2)^k / k!), Horner with fused
@@ -73,13 +77,26 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
 }
 
 struct SmpShared {
-    unsigned long long hist[NBUCKET];
+    // Bucket sums as two 32-bit words (a sum reaches 2^40): native 32-bit
+    // shared-memory atomics on the low word, a carry counted in the high word.
+    uint32_t hlo[NBUCKET];
+    uint32_t hhi[NBUCKET];
     unsigned long long wsum[32];
     float wf[32];
     int wi[32];
     unsigned long long bcast[4];
     int ibcast[4];
 };
+
+__device__ __forceinline__ unsigned long long hist_get(const SmpShared &sm, int h) {
+    return ((unsigned long long)sm.hhi[h] << 32) | sm.hlo[h];
+}
+__device__ __forceinline__ void hist_clear(SmpShared &sm) {
+    for (int i = threadIdx.x; i < NBUCKET; i += blockDim.x) {
+        sm.hlo[i] = 0u;
+        sm.hhi[i] = 0u;
+    }
+}
 
 // Exclusive prefix sum over the CTA (thread order) of a 64-bit value; returns
 // the prefix and writes the total to *total.
@@ -116,17 +133,17 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
     return tot;
 }
 
-// Over the 4096 (+1 top) buckets of sm.hist: the largest bucket index h with
+// Over the 4096 (+1 top) buckets of the histogram: the largest bucket index h with
 // base + sum_{h' >= h} hist[h'] >= target (-1 if none); *above receives
 // base + sum_{h' > h} hist[h'].  nb = number of buckets (4097 or 4096).
 __device__ __forceinline__ int find_cut(SmpShared &sm, int nb, unsigned long long base,
                                         unsigned long long target, unsigned long long *above) {
     // thread t owns buckets [4t, 4t + 4); bucket 4096 (if nb == 4097) is added to base.
     const int t = threadIdx.x;
-    unsigned long long top = (nb == NBUCKET) ? sm.hist[4096] : 0ull;
+    unsigned long long top = (nb == NBUCKET) ? hist_get(sm, 4096) : 0ull;
     unsigned long long mine = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mine += sm.hist[4 * t + j];
+    for (int j = 0; j < 4; ++j) mine += hist_get(sm, 4 * t + j);
     // suffix sum: total - inclusive prefix
     unsigned long long total;
     const unsigned long long excl = block_excl_scan(mine, sm, &total);
@@ -146,7 +163,7 @@ __device__ __forceinline__ int find_cut(SmpShared &sm, int nb, unsigned long lon
         for (int j = 3; j >= 0; --j) {
             const int h = 4 * t + j;
             const unsigned long long above_h = run;
-            run += sm.hist[h];
+            run += hist_get(sm, h);
             if (run >= target && above_h < target) {
                 sm.ibcast[0] = h;  // unique: the suffix sum crosses target exactly once
                 sm.bcast[0] = above_h;
@@ -160,7 +177,29 @@ __device__ __forceinline__ int find_cut(SmpShared &sm, int nb, unsigned long lon
     return h;
 }
 
-// Same with counts instead of sums (hist holds counts).
+// hist[key] += val for the lanes with live set.  The weights of a row crowd
+// into few low buckets when the logits are spread wide, and per-lane atomics on
+// one address serialise, so the lanes that share lane 0's key are summed first
+// (__reduce_add_sync; val <= 2^24, so 32 of them fit in 32 bits) and added
+// once; the others add their own value (distinct keys hit distinct words).
+// Sums use native 32-bit shared-memory atomics on the low word, a wrap of it
+// is carried into the high word.  Called by all 32 lanes.
+__device__ __forceinline__ void hist_add(SmpShared &sm, uint32_t key, uint32_t val) {
+    const uint32_t old = atomicAdd(&sm.hlo[key], val);
+    if (old + val < old) atomicAdd(&sm.hhi[key], 1u);  // the low word wrapped
+}
+__device__ __forceinline__ void hist_add_warp(SmpShared &sm, uint32_t key, uint32_t val, bool live) {
+    const uint32_t k = live ? key : 0xffffffffu;
+    const uint32_t k0 = __shfl_sync(0xffffffffu, k, 0);
+    const bool same = k == k0;
+    const uint32_t gsum = __reduce_add_sync(0xffffffffu, same ? val : 0u);
+    if ((threadIdx.x & 31) == 0) {
+        if (live) hist_add(sm, key, gsum);
+    } else if (!same && live) {
+        hist_add(sm, key, val);
+    }
+}
+
 __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SmpShared &sm = *reinterpret_cast<SmpShared *>(smem_raw);
@@ -182,11 +221,20 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     if (sp.greedy || !(sp.temperature > 0.0f)) {
         float best = -INFINITY;
         int bi = 0x7fffffff;
-        for (int i = tid; i < V; i += SMP_THREADS) {
-            const float v = lg[i];
-            if (v > best || (v == best && i < bi)) {
-                best = v;
-                bi = i;
+        for (int i0 = 0; i0 < V; i0 += SMP_STEP) {
+            float v[SMP_U];
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = i0 + u * SMP_THREADS + tid;
+                v[u] = i < V ? lg[i] : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {  // ascending i per thread: ">" keeps the lowest index
+                const int i = i0 + u * SMP_THREADS + tid;
+                if (i < V && (v[u] > best || (v[u] == best && i < bi))) {
+                    best = v[u];
+                    bi = i;
+                }
             }
         }
 #pragma unroll
@@ -218,16 +266,31 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
 
     float *occ = p.occ + (size_t)slot * V;
     float *lp = p.lpen + (size_t)b * V;
-    // ---- pass A: penalty and max
+    // ---- pass A: penalty and max; the occurrence counts are decayed here
+    // (every row draws a token: the row maximum always keeps weight 2^24), the
+    // drawn token's +1 is added at the end.
     float mx = -INFINITY;
-    for (int i = tid; i < V; i += SMP_THREADS) {
-        const float o = occ[i];
-        const float pres = o > 0.0f ? sp.presence : 0.0f;
-        float t = __fmul_rn(o, sp.frequency);
-        t = __fadd_rn(pres, t);
-        const float l = __fsub_rn(lg[i], t);
-        lp[i] = l;
-        mx = fmaxf(mx, l);
+    for (int i0 = 0; i0 < V; i0 += SMP_STEP) {
+        float lv[SMP_U], ov[SMP_U];
+#pragma unroll
+        for (int u = 0; u < SMP_U; ++u) {
+            const int i = i0 + u * SMP_THREADS + tid;
+            lv[u] = i < V ? lg[i] : 0.0f;
+            ov[u] = i < V ? occ[i] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < SMP_U; ++u) {
+            const int i = i0 + u * SMP_THREADS + tid;
+            if (i < V) {
+                const float pres = ov[u] > 0.0f ? sp.presence : 0.0f;
+                float t = __fmul_rn(ov[u], sp.frequency);
+                t = __fadd_rn(pres, t);
+                const float l = __fsub_rn(lv[u], t);
+                lp[i] = l;
+                mx = fmaxf(mx, l);
+                occ[i] = __fmul_rn(ov[u], sp.penalty_decay);
+            }
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -243,7 +306,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     __syncthreads();
 
     // ---- pass B: weight sums per (q1 >> 12) bucket
-    for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+    hist_clear(sm);
     __syncthreads();
     // At temperature 1 the draw weights are the q1 weights, so they are
     // computed once here and stored over the row's penalised logits; the later
@@ -251,11 +314,24 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     const bool t1 = sp.temperature == 1.0f;
     uint32_t *lq = reinterpret_cast<uint32_t *>(lp);
     unsigned long long q1loc = 0;
-    for (int i = tid; i < V; i += SMP_THREADS) {
-        const uint32_t q = qweight(lp[i], m, 1.0f);
-        if (t1) lq[i] = q;
-        q1loc += q;
-        if (q) atomicAdd(&sm.hist[q >> 12], (unsigned long long)q);
+    for (int i0 = 0; i0 < V; i0 += SMP_STEP) {  // warp-uniform trip count
+        float lv[SMP_U];
+#pragma unroll
+        for (int u = 0; u < SMP_U; ++u) {
+            const int i = i0 + u * SMP_THREADS + tid;
+            lv[u] = i < V ? lp[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < SMP_U; ++u) {
+            const int i = i0 + u * SMP_THREADS + tid;
+            uint32_t q = 0;
+            if (i < V) {
+                q = qweight(lv[u], m, 1.0f);
+                if (t1) lq[i] = q;
+                q1loc += q;
+            }
+            hist_add_warp(sm, q >> 12, q, q != 0u);
+        }
     }
     const unsigned long long Q1 = block_sum_u64(q1loc, sm);
     unsigned long long target = (unsigned long long)ceil(__dmul_rn((double)sp.top_p, (double)Q1));
@@ -263,12 +339,21 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     if (target > Q1) target = Q1;
     unsigned long long above;
     const int hb = find_cut(sm, NBUCKET, 0ull, target, &above);
+    // q1 of element i, read back (temperature 1) or recomputed
+    auto q1_at = [&](int i) -> uint32_t { return t1 ? lq[i] : qweight(lp[i], m, 1.0f); };
     // ---- pass C: low 12 bits within bucket hb
-    for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+    hist_clear(sm);
     __syncthreads();
-    for (int i = tid; i < V; i += SMP_THREADS) {
-        const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
-        if ((int)(q >> 12) == hb && q) atomicAdd(&sm.hist[q & 4095u], (unsigned long long)q);
+    for (int i0 = 0; i0 < V; i0 += SMP_STEP) {
+        uint32_t qv[SMP_U];
+#pragma unroll
+        for (int u = 0; u < SMP_U; ++u) {
+            const int i = i0 + u * SMP_THREADS + tid;
+            qv[u] = i < V ? q1_at(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < SMP_U; ++u)
+            hist_add_warp(sm, qv[u] & 4095u, qv[u], (int)(qv[u] >> 12) == hb && qv[u] != 0u);
     }
     __syncthreads();
     unsigned long long above2;
@@ -281,17 +366,34 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     unsigned long long need_ties = 0;
     if (use_k) {
         const unsigned long long K = (unsigned long long)sp.top_k;
-        for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+        hist_clear(sm);
         __syncthreads();
-        for (int i = tid; i < V; i += SMP_THREADS) atomicAdd(&sm.hist[(t1 ? lq[i] : qweight(lp[i], m, 1.0f)) >> 12], 1ull);
+        for (int i0 = 0; i0 < V; i0 += SMP_STEP) {
+            uint32_t qv[SMP_U];
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = i0 + u * SMP_THREADS + tid;
+                qv[u] = i < V ? q1_at(i) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) hist_add_warp(sm, qv[u] >> 12, 1u, i0 + u * SMP_THREADS + tid < V);
+        }
         __syncthreads();
         unsigned long long cabove;
         const int hk = find_cut(sm, NBUCKET, 0ull, K, &cabove);
-        for (int i = tid; i < NBUCKET; i += SMP_THREADS) sm.hist[i] = 0ull;
+        hist_clear(sm);
         __syncthreads();
-        for (int i = tid; i < V; i += SMP_THREADS) {
-            const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
-            if ((int)(q >> 12) == hk) atomicAdd(&sm.hist[q & 4095u], 1ull);
+        for (int i0 = 0; i0 < V; i0 += SMP_STEP) {
+            uint32_t qv[SMP_U];
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = i0 + u * SMP_THREADS + tid;
+                qv[u] = i < V ? q1_at(i) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u)
+                hist_add_warp(sm, qv[u] & 4095u, 1u,
+                              i0 + u * SMP_THREADS + tid < V && (int)(qv[u] >> 12) == hk);
         }
         __syncthreads();
         unsigned long long cgt;
@@ -300,66 +402,114 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
         need_ties = K - cgt;  // elements equal to tk to keep (lowest indices first)
     }
 
-    // ---- pass D: kept set, qT, exclusive scan in index order, draw, pick
-    const int C = (V + SMP_THREADS - 1) / SMP_THREADS;
-    const int i_lo = tid * C, i_hi = min(V, i_lo + C);
-    unsigned long long tie_base = 0;
+    // ---- pass D: kept set, qT, exclusive scan in index order, draw, pick.
+    // Warp w owns the contiguous range [w * CW, (w + 1) * CW) and walks it in
+    // blocks of 32 consecutive elements (one coalesced load per block), so the
+    // index order is (warp, block, lane).  A tie with t_k is kept while fewer
+    // than need_ties ties precede it in that order.
+    const int lane = tid & 31, w = tid >> 5;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int CW = ((V + 31) / 32 + 31) / 32 * 32;
+    const int w_lo = w * CW, w_hi = min(V, w_lo + CW);
+    const int nblk = w_hi > w_lo ? (w_hi - w_lo + 31) / 32 : 0;  // warp-uniform
+    unsigned long long tie_base = 0;  // ties before this warp's range
     if (use_k) {
-        unsigned long long ties = 0;
-        for (int i = i_lo; i < i_hi; ++i) ties += ((t1 ? lq[i] : qweight(lp[i], m, 1.0f)) == tk);
+        unsigned ties = 0;
+        for (int k0 = 0; k0 < nblk; k0 += SMP_U) {
+            uint32_t qv[SMP_U];
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = w_lo + (k0 + u) * 32 + lane;
+                qv[u] = (k0 + u < nblk && i < w_hi) ? q1_at(i) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = w_lo + (k0 + u) * 32 + lane;
+                ties += (k0 + u < nblk && i < w_hi && qv[u] == tk) ? 1u : 0u;
+            }
+        }
+        const unsigned wt = __reduce_add_sync(0xffffffffu, ties);
         unsigned long long tt;
-        tie_base = block_excl_scan(ties, sm, &tt);
+        tie_base = __shfl_sync(0xffffffffu, block_excl_scan(lane == 0 ? (unsigned long long)wt : 0ull, sm, &tt), 0);
     }
+    // kept weight of element i with value q; *tie_seen counts the warp's ties so far
+    auto kept_weight = [&](int i, bool in, uint32_t q, unsigned long long *tie_seen) -> unsigned long long {
+        bool keep = in && q >= tp;
+        if (use_k) {
+            const bool tie = in && q == tk;
+            const unsigned tb = __ballot_sync(0xffffffffu, tie);
+            const unsigned long long rank = *tie_seen + (unsigned long long)__popc(tb & lt_mask);
+            keep = keep && (q > tk || (tie && rank < need_ties));
+            *tie_seen += (unsigned long long)__popc(tb);
+        }
+        if (!keep) return 0ull;
+        return t1 ? (unsigned long long)q : (unsigned long long)qweight(lp[i], m, sp.temperature);
+    };
     unsigned long long rloc = 0;
     {
         unsigned long long tie_seen = tie_base;
-        for (int i = i_lo; i < i_hi; ++i) {
-            const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
-            bool keep = q >= tp;
-            if (use_k) {
-                const bool tie = (q == tk);
-                keep = keep && (q > tk || (tie && tie_seen < need_ties));
-                tie_seen += tie;
+        for (int k0 = 0; k0 < nblk; k0 += SMP_U) {
+            uint32_t qv[SMP_U];
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = w_lo + (k0 + u) * 32 + lane;
+                qv[u] = (k0 + u < nblk && i < w_hi) ? q1_at(i) : 0u;
             }
-            if (keep) rloc += t1 ? q : qweight(lp[i], m, sp.temperature);
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = w_lo + (k0 + u) * 32 + lane;
+                if (k0 + u < nblk) rloc += kept_weight(i, i < w_hi, qv[u], &tie_seen);
+            }
         }
     }
+    unsigned long long wsum = rloc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     unsigned long long R;
-    const unsigned long long rbase = block_excl_scan(rloc, sm, &R);
+    const unsigned long long rbase =
+        __shfl_sync(0xffffffffu, block_excl_scan(lane == 0 ? wsum : 0ull, sm, &R), 0);  // before this warp
     const unsigned long long nd = p.ndraw[slot];
     uint32_t ctr[4] = {(uint32_t)nd, (uint32_t)(nd >> 32), 0u, 0u};
     philox4x32_10(ctr, (uint32_t)sp.seed, (uint32_t)(sp.seed >> 32));
-    const unsigned long long u = (unsigned long long)ctr[0] | ((unsigned long long)ctr[1] << 32);
-    const unsigned long long r = __umul64hi(u, R);
+    const unsigned long long u64 = (unsigned long long)ctr[0] | ((unsigned long long)ctr[1] << 32);
+    const unsigned long long r = __umul64hi(u64, R);
     if (tid == 0) sm.ibcast[1] = -1;
     __syncthreads();
-    if (rloc > 0 && rbase <= r && r < rbase + rloc) {
+    if (wsum > 0 && rbase <= r && r < rbase + wsum) {  // warp-uniform: this warp holds the draw
         unsigned long long acc = rbase, tie_seen = tie_base;
-        for (int i = i_lo; i < i_hi; ++i) {
-            const uint32_t q = (t1 ? lq[i] : qweight(lp[i], m, 1.0f));
-            bool keep = q >= tp;
-            if (use_k) {
-                const bool tie = (q == tk);
-                keep = keep && (q > tk || (tie && tie_seen < need_ties));
-                tie_seen += tie;
+        bool found = false;
+        for (int k0 = 0; k0 < nblk && !found; k0 += SMP_U) {
+            uint32_t qv[SMP_U];
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                const int i = w_lo + (k0 + u) * 32 + lane;
+                qv[u] = (k0 + u < nblk && i < w_hi) ? q1_at(i) : 0u;
             }
-            if (!keep) continue;
-            acc += t1 ? q : qweight(lp[i], m, sp.temperature);
-            if (acc > r) {
-                sm.ibcast[1] = i;
-                break;
+#pragma unroll
+            for (int u = 0; u < SMP_U; ++u) {
+                if (found || k0 + u >= nblk) continue;  // warp-uniform conditions
+                const int i = w_lo + (k0 + u) * 32 + lane;
+                const unsigned long long kw = kept_weight(i, i < w_hi, qv[u], &tie_seen);
+                unsigned long long incl = kw;  // inclusive scan over the block's lanes
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, kw > 0 && acc + incl > r);
+                if (hit) {
+                    if (lane == __ffs(hit) - 1) sm.ibcast[1] = i;
+                    found = true;
+                }
+                acc += __shfl_sync(0xffffffffu, incl, 31);
             }
         }
     }
     __syncthreads();
     const int tok = sm.ibcast[1];
-    // ---- pass E: occurrence decay and count
-    if (tok >= 0) {
-        for (int i = tid; i < V; i += SMP_THREADS) occ[i] = __fmul_rn(occ[i], sp.penalty_decay);
-        __syncthreads();
-        if (tid == 0) occ[tok] = __fadd_rn(occ[tok], 1.0f);
-    }
+    // ---- pass E: count the drawn token (the decay was applied in pass A)
     if (tid == 0) {
+        if (tok >= 0) occ[tok] = __fadd_rn(occ[tok], 1.0f);
         p.next[b] = tok >= 0 ? tok : 0;
         if (tok < 0) atomicOr(p.err, ERR_CONFIG);
         p.ndraw[slot] = nd + 1ull;
