@@ -55,16 +55,17 @@ __device__ __forceinline__ bool epi_store(const GemmSeg &s, int n, int b, float 
 
 // Epilogue of one finished accumulator (one weight row n per thread, npad slot
 // columns in TMEM): the kind is dispatched once, then a straight-line loop per
-// 32-column chunk.  Split items store raw fp32 partials (slab `split`).  Every
+// 32-column chunk; the two epilogue warps of a TMEM lane quarter take
+// alternate chunks (c0 = 0 or 32).  Split items store raw fp32 partials (slab `split`).  Every
 // lane executes the TMEM loads (they are warp-collective); stores are guarded.
 template <int KIND>
 __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split, int npad,
-                                        int B) {
+                                        int B, int c0) {
     const bool live = n < sg.rows;
     float bias = 0.0f;
     if ((KIND == EPI_DECAY || KIND == EPI_SIGMOID_BIAS) && live) bias = __half2float(sg.bias[n]);
     bool nz = false;
-    for (int cb = 0; cb < npad; cb += 32) {
+    for (int cb = c0; cb < npad; cb += 64) {
         float v[32];
         if (valid) {
             if (cb + 32 <= npad) {
@@ -129,17 +130,17 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
 }
 
 __device__ __forceinline__ bool epi_item(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split, int npad,
-                                         int B) {
-    if (sg.S > 1) return epi_run<-1>(sg, taddr, valid, n, split, npad, B);
+                                         int B, int c0) {
+    if (sg.S > 1) return epi_run<-1>(sg, taddr, valid, n, split, npad, B, c0);
     switch (sg.epi) {
-        case EPI_F32: return epi_run<EPI_F32>(sg, taddr, valid, n, split, npad, B);
-        case EPI_F16: return epi_run<EPI_F16>(sg, taddr, valid, n, split, npad, B);
-        case EPI_F16_TANH: return epi_run<EPI_F16_TANH>(sg, taddr, valid, n, split, npad, B);
-        case EPI_F16_SIGMOID: return epi_run<EPI_F16_SIGMOID>(sg, taddr, valid, n, split, npad, B);
-        case EPI_DECAY: return epi_run<EPI_DECAY>(sg, taddr, valid, n, split, npad, B);
-        case EPI_SIGMOID_BIAS: return epi_run<EPI_SIGMOID_BIAS>(sg, taddr, valid, n, split, npad, B);
-        case EPI_RESID: return epi_run<EPI_RESID>(sg, taddr, valid, n, split, npad, B);
-        case EPI_RELU2: return epi_run<EPI_RELU2>(sg, taddr, valid, n, split, npad, B);
+        case EPI_F32: return epi_run<EPI_F32>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_F16: return epi_run<EPI_F16>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_F16_TANH: return epi_run<EPI_F16_TANH>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_F16_SIGMOID: return epi_run<EPI_F16_SIGMOID>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_DECAY: return epi_run<EPI_DECAY>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_SIGMOID_BIAS: return epi_run<EPI_SIGMOID_BIAS>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_RESID: return epi_run<EPI_RESID>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_RELU2: return epi_run<EPI_RELU2>(sg, taddr, valid, n, split, npad, B, c0);
         default: return false;
     }
 }
@@ -178,7 +179,11 @@ __device__ __forceinline__ bool stage_skipped(const uint32_t *flags, int kb) {
 constexpr int MAX_NZ_BLOCKS = 1024;  // d_ffn / 64
 
 
-__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+constexpr int EPI_WARPS = 8;                       // two per TMEM lane quarter
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int GEMM_TC_THREADS = 64 + EPI_THREADS;
+
+__global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     // Segment descriptors and sparsity flags are staged in shared memory and the
     // scalars in registers: the parameter block is only addressed for the tensor
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     uint64_t *acc_empty = acc_full + 2;  // [2]
     uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    volatile uint32_t *nzq = tmem_slot + 3;  // [4]
+    volatile uint32_t *nzq = tmem_slot + 3;  // [8]: (lane quarter, column half)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 128);
+            mbar_init(&acc_empty[i], EPI_THREADS);
         }
         mbar_init(&flags_ready, 1);
         *abort_flag = 0u;
@@ -348,13 +353,14 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         pdl_wait();
         const int qd = warp & 3;              // TMEM lane quarter of this warp
         const int row = qd * 32 + lane;       // accumulator row = weight row within the tile
-        const int et = threadIdx.x - 64;      // 0..127
+        const int et = threadIdx.x - 64;      // 0..EPI_THREADS-1
+        const int half = et >> 7;             // column chunks half, half + 2, ... of each accumulator
         uint32_t *nz_out = p.nz_out;
         if (has_skip) {  // stage the k-block flags written by the preceding kernel
             const int nkb = sseg[0].kb < MAX_NZ_BLOCKS ? sseg[0].kb : MAX_NZ_BLOCKS;  // padded count
             const int nreal = (sseg[0].K + GEMM_TILE_K - 1) / GEMM_TILE_K;             // flags written
-            for (int j = et; j < nkb; j += 128) snz[j] = j < nreal ? p.nz_skip[j] : 0u;
-            named_bar(1, 128);
+            for (int j = et; j < nkb; j += EPI_THREADS) snz[j] = j < nreal ? p.nz_skip[j] : 0u;
+            named_bar(1, EPI_THREADS);
             if (et == 0) mbar_arrive(&flags_ready);
         }
         int n = 0;
@@ -368,9 +374,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             // thread 0 waits and tells the others, so that all 128 threads take
             // the same path through the named barriers below
             if (et == 0) s_ok = mbar_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u, abort_flag) ? 1u : 0u;
-            named_bar(3, 128);
+            named_bar(3, EPI_THREADS);
             const bool ok_wait = s_ok != 0u;
-            named_bar(3, 128);
+            named_bar(3, EPI_THREADS);
             if (!ok_wait) {
                 if (et == 0) {
                     *abort_flag = 1u;
@@ -382,27 +388,29 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
             const int nrow = it.tile * GEMM_TILE_M + row;
-            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B);
+            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B, half * 32);
             tc_fence_before();
             mbar_arrive(&acc_empty[buf]);
             if (sg.epi == EPI_RELU2 && sg.S == 1 && nz_out != nullptr) {
                 const unsigned bal = __ballot_sync(0xffffffffu, nzany);
-                if (lane == 0) nzq[qd] = bal ? 1u : 0u;
-                named_bar(2, 128);
+                if (lane == 0) nzq[qd + 4 * half] = bal ? 1u : 0u;
+                named_bar(2, EPI_THREADS);
                 if (et == 0) {
                     const int blk0 = it.tile * 2;
                     const int nblk = (sg.rows + 63) / 64;
-                    const uint32_t f0 = nzq[0] | nzq[1], f1 = nzq[2] | nzq[3];
+                    const uint32_t f0 = nzq[0] | nzq[1] | nzq[4] | nzq[5];  // rows 0-63 of the tile
+                    const uint32_t f1 = nzq[2] | nzq[3] | nzq[6] | nzq[7];  // rows 64-127
                     if (blk0 < nblk) nz_out[blk0] = f0;
                     if (blk0 + 1 < nblk) nz_out[blk0 + 1] = f1;
                     const unsigned long long nnz = (blk0 < nblk ? f0 : 0u) + (blk0 + 1 < nblk ? f1 : 0u);
                     if (p.nz_count && nnz) atomicAdd(p.nz_count, nnz);
                 }
-                named_bar(2, 128);
+                named_bar(2, EPI_THREADS);
             }
         }
     }
 
+    __syncwarp();  // warps 0 and 1 reconverge (lane 0 ran the producer / MMA loop)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -432,7 +440,7 @@ void launch_gemm_tc(const GemmParams &p, int grid, size_t smem, const LaunchCfg 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(GEMM_TC_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = lc.stream;
     cudaLaunchAttribute at[1];
