@@ -53,11 +53,39 @@ __device__ __forceinline__ bool epi_store(const GemmSeg &s, int n, int b, float 
     return false;
 }
 
+// Epilogue warps: EPI_GROUPS per TMEM lane quarter (a warp may only read its
+// own quarter's 32 lanes); group g of a quarter takes the column chunks
+// g, g + EPI_GROUPS, ... of EPI_CW slot columns each, so that a wide batch's
+// epilogue is spread over many warps instead of running as one latency chain
+// per sub-partition.
+constexpr int EPI_GROUPS = 4;
+constexpr int EPI_WARPS = 4 * EPI_GROUPS;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int EPI_CW = 16;
+constexpr int GEMM_TC_THREADS = 64 + EPI_THREADS;
+
+// One chunk of accumulator columns into registers (a 32-column chunk may be the
+// 16-column tail of the accumulator: the rest reads as zero).
+__device__ __forceinline__ void chunk_ld(uint32_t taddr, float (&v)[16], bool) { tmem_ld16(taddr, v); }
+__device__ __forceinline__ void chunk_ld(uint32_t taddr, float (&v)[32], bool full) {
+    if (full) {
+        tmem_ld32(taddr, v);
+    } else {
+        float h[16];
+        tmem_ld16(taddr, h);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            v[q] = h[q];
+            v[q + 16] = 0.0f;
+        }
+    }
+}
+
 // Epilogue of one finished accumulator (one weight row n per thread, npad slot
-// columns in TMEM): the kind is dispatched once, then a straight-line loop per
-// 32-column chunk; the two epilogue warps of a TMEM lane quarter take
-// alternate chunks (c0 = 0 or 32).  Split items store raw fp32 partials (slab `split`).  Every
-// lane executes the TMEM loads (they are warp-collective); stores are guarded.
+// columns in TMEM; npad is a multiple of 16): the kind is dispatched once, then
+// a straight-line loop per chunk of EPI_CW columns starting at column c0.
+// Split items store raw fp32 partials (slab `split`).  Every lane executes the
+// TMEM loads (they are warp-collective); stores are guarded.
 template <int KIND>
 __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split, int npad,
                                         int B, int c0) {
@@ -65,43 +93,33 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
     float bias = 0.0f;
     if ((KIND == EPI_DECAY || KIND == EPI_SIGMOID_BIAS) && live) bias = __half2float(sg.bias[n]);
     bool nz = false;
-    for (int cb = c0; cb < npad; cb += 64) {
-        float v[32];
+    for (int cb = c0; cb < npad; cb += EPI_GROUPS * EPI_CW) {
+        float v[EPI_CW];
         if (valid) {
-            if (cb + 32 <= npad) {
-                tmem_ld32(taddr + (uint32_t)cb, v);
-            } else {
-                float h[16];
-                tmem_ld16(taddr + (uint32_t)cb, h);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    v[q] = h[q];
-                    v[q + 16] = 0.0f;
-                }
-            }
+            chunk_ld(taddr + (uint32_t)cb, v, cb + EPI_CW <= npad);
         } else {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = 0.0f;
+            for (int q = 0; q < EPI_CW; ++q) v[q] = 0.0f;
         }
         if (!live) continue;
-        const int nq = min(32, B - cb);
+        const int nq = min(EPI_CW, B - cb);
         if (KIND == -1) {  // raw fp32 partial
             float *out = (float *)sg.out + (size_t)split * sg.split_stride + (size_t)cb * sg.ldo + n;
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
+            for (int q = 0; q < EPI_CW; ++q)
                 if (q < nq) out[(size_t)q * sg.ldo] = v[q];
         } else if (KIND == EPI_RESID) {
             float *out = (float *)sg.out + (size_t)cb * sg.ldo + n;
-            float old[32];
+            float old[EPI_CW];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) old[q] = q < nq ? out[(size_t)q * sg.ldo] : 0.0f;
+            for (int q = 0; q < EPI_CW; ++q) old[q] = q < nq ? out[(size_t)q * sg.ldo] : 0.0f;
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
+            for (int q = 0; q < EPI_CW; ++q)
                 if (q < nq) out[(size_t)q * sg.ldo] = old[q] + v[q];
         } else if (KIND == EPI_F32 || KIND == EPI_DECAY || KIND == EPI_SIGMOID_BIAS) {
             float *out = (float *)sg.out + (size_t)cb * sg.ldo + n;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
+            for (int q = 0; q < EPI_CW; ++q) {
                 float y = v[q];
                 if (KIND == EPI_DECAY) y = rwkv_decay(bias + y);
                 if (KIND == EPI_SIGMOID_BIAS) y = fast_sigmoid(bias + y);
@@ -110,7 +128,7 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
         } else {  // fp16 outputs
             __half *out = (__half *)sg.out + (size_t)cb * sg.ldo + n;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
+            for (int q = 0; q < EPI_CW; ++q) {
                 float y = v[q];
                 if (KIND == EPI_F16_TANH) y = fast_tanh(y);
                 if (KIND == EPI_F16_SIGMOID) y = fast_sigmoid(y);
@@ -179,10 +197,6 @@ __device__ __forceinline__ bool stage_skipped(const uint32_t *flags, int kb) {
 constexpr int MAX_NZ_BLOCKS = 1024;  // d_ffn / 64
 
 
-constexpr int EPI_WARPS = 8;                       // two per TMEM lane quarter
-constexpr int EPI_THREADS = EPI_WARPS * 32;
-constexpr int GEMM_TC_THREADS = 64 + EPI_THREADS;
-
 __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     // Segment descriptors and sparsity flags are staged in shared memory and the
@@ -206,7 +220,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
     uint64_t *acc_empty = acc_full + 2;  // [2]
     uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    volatile uint32_t *nzq = tmem_slot + 3;  // [8]: (lane quarter, column half)
+    uint32_t *nzf = tmem_slot + 2;  // [2]: some output of tile rows 0-63 / 64-127 was nonzero
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -226,6 +240,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
         }
         mbar_init(&flags_ready, 1);
         *abort_flag = 0u;
+        nzf[0] = nzf[1] = 0u;
         fence_barrier_init();
     }
     __syncthreads();
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
         const int qd = warp & 3;              // TMEM lane quarter of this warp
         const int row = qd * 32 + lane;       // accumulator row = weight row within the tile
         const int et = threadIdx.x - 64;      // 0..EPI_THREADS-1
-        const int half = et >> 7;             // column chunks half, half + 2, ... of each accumulator
+        const int grp = et >> 7;              // column-chunk group within the lane quarter
         uint32_t *nz_out = p.nz_out;
         if (has_skip) {  // stage the k-block flags written by the preceding kernel
             const int nkb = sseg[0].kb < MAX_NZ_BLOCKS ? sseg[0].kb : MAX_NZ_BLOCKS;  // padded count
@@ -388,18 +403,18 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
             const int nrow = it.tile * GEMM_TILE_M + row;
-            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B, half * 32);
+            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B, grp * EPI_CW);
             tc_fence_before();
             mbar_arrive(&acc_empty[buf]);
             if (sg.epi == EPI_RELU2 && sg.S == 1 && nz_out != nullptr) {
                 const unsigned bal = __ballot_sync(0xffffffffu, nzany);
-                if (lane == 0) nzq[qd + 4 * half] = bal ? 1u : 0u;
+                if (lane == 0 && bal) atomicOr(&nzf[qd >> 1], 1u);
                 named_bar(2, EPI_THREADS);
                 if (et == 0) {
                     const int blk0 = it.tile * 2;
                     const int nblk = (sg.rows + 63) / 64;
-                    const uint32_t f0 = nzq[0] | nzq[1] | nzq[4] | nzq[5];  // rows 0-63 of the tile
-                    const uint32_t f1 = nzq[2] | nzq[3] | nzq[6] | nzq[7];  // rows 64-127
+                    const uint32_t f0 = ((volatile uint32_t *)nzf)[0], f1 = ((volatile uint32_t *)nzf)[1];
+                    nzf[0] = nzf[1] = 0u;  // for the next item, after the barrier below
                     if (blk0 < nblk) nz_out[blk0] = f0;
                     if (blk0 + 1 < nblk) nz_out[blk0 + 1] = f1;
                     const unsigned long long nnz = (blk0 < nblk ? f0 : 0u) + (blk0 + 1 < nblk ? f1 : 0u);
