@@ -38,18 +38,38 @@ __device__ __forceinline__ void st8f(float *p, const float (&f)[8]) {
 }
 
 // x[8] += sum over j < nsplit of part[j * stride + off .. +8], slabs added in
-// order j = 0, 1, ... (loads issued four slabs at a time).
+// order j = 0, 1, ... (the loads of up to eight slabs are issued together).
 __device__ __forceinline__ void add_slabs(float (&x)[8], const float *part, int nsplit, long long stride, size_t off) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     int j = 0;
-    for (; j + 4 <= nsplit; j += 4) {
+    for (; j + 8 <= nsplit; j += 8) {
+        float t[8][8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ld8f(part + (size_t)(j + u) * stride + off, t[u]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] += t[u][k];
+    }
+    if (j + 4 <= nsplit) {
         float t[4][8];
 #pragma unroll
         for (int u = 0; u < 4; ++u) ld8f(part + (size_t)(j + u) * stride + off, t[u]);
+        float t2[3][8];
+        const int rest = nsplit - j - 4;  // 0..3 more slabs, loaded alongside
+#pragma unroll
+        for (int u = 0; u < 3; ++u)
+            if (u < rest) ld8f(part + (size_t)(j + 4 + u) * stride + off, t2[u]);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
             for (int k = 0; k < 8; ++k) acc[k] += t[u][k];
+#pragma unroll
+        for (int u = 0; u < 3; ++u)
+            if (u < rest)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[k] += t2[u][k];
+        j = nsplit;
     }
     for (; j < nsplit; ++j) {
         float t[8];
@@ -61,11 +81,14 @@ __device__ __forceinline__ void add_slabs(float (&x)[8], const float *part, int 
     for (int k = 0; k < 8; ++k) x[k] += acc[k];
 }
 
-// Sum over the CTA.  `red` holds 32 floats.
+// Sum over the CTA with one barrier.  `red` holds 32 floats.  A thread may
+// write them while others still read the previous sum from the same buffer,
+// so consecutive sums alternate between two buffers: a thread writes buffer A
+// again only after the barrier of the sum on buffer B, which every thread
+// reaches after reading A.
 __device__ __forceinline__ float block_sum(float v, float *red) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_sum(v);
-    __syncthreads();
     if (lane == 0) red[w] = v;
     __syncthreads();
     float t = 0.0f;
@@ -74,7 +97,8 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 }
 
 // In-place LayerNorm of the d values held 8 per thread (inactive threads hold
-// zeros): (x - mean) / sqrt(var + 1e-5) * w + b, biased variance.
+// zeros): (x - mean) / sqrt(var + 1e-5) * w + b, biased variance.  `red` holds
+// 64 floats; called once per kernel.
 __device__ __forceinline__ void ln8(float (&v)[8], bool act, int d, const uint4 &w4, const uint4 &b4, float *red) {
     float s = 0.0f;
 #pragma unroll
@@ -88,7 +112,7 @@ __device__ __forceinline__ void ln8(float (&v)[8], bool act, int d, const uint4 
             q += t * t;
         }
     }
-    const float var = block_sum(q, red) / (float)d;
+    const float var = block_sum(q, red + 32) / (float)d;
     const float rs = 1.0f / sqrtf(var + 1e-5f);
     float w[8], b[8];
     h8_to_f(w4, w);
@@ -102,7 +126,7 @@ __device__ __forceinline__ void ln8(float (&v)[8], bool act, int d, const uint4 
 // repeated slots with a bitmap in shared memory.
 __global__ void embed_kernel(const ElemParams p) {
     extern __shared__ uint32_t bitmap[];
-    __shared__ float red[32];
+    __shared__ float red[64];
     pdl_wait();
     pdl_launch();
     const int b = blockIdx.x;
@@ -144,7 +168,7 @@ __global__ void embed_kernel(const ElemParams p) {
 // earlier) are fetched before the dependency wait.
 template <int NMIX>
 __global__ void ln_mix_kernel(const ElemParams p) {
-    __shared__ float red[32];
+    __shared__ float red[64];
     const int b = blockIdx.x;
     const int i0 = threadIdx.x * 8;
     const bool act = i0 < p.d;
@@ -185,7 +209,7 @@ __global__ void ln_mix_kernel(const ElemParams p) {
 
 // xo[0][b] = fp16(LN_out(x[b])): the input of the head projection.
 __global__ void ln_out_kernel(const ElemParams p) {
-    __shared__ float red[32];
+    __shared__ float red[64];
     const int b = blockIdx.x;
     const int i0 = threadIdx.x * 8;
     const bool act = i0 < p.d;
@@ -361,7 +385,7 @@ __device__ __forceinline__ void ln_row(const ElemParams &p, int t, int i0, bool 
 
 template <int NMIX>
 __global__ void ln_mix_prefill_kernel(const ElemParams p) {
-    __shared__ float red[32];
+    __shared__ float red[64];
     const int t = blockIdx.x, n = gridDim.x;
     const int i0 = threadIdx.x * 8;
     const bool act = i0 < p.d;
