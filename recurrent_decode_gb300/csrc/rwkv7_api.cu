@@ -220,12 +220,25 @@ int make_wmap(rwkv7_ctx *c, int kind) {
     return make_map(c, &c->wmap1[kind], c->w[kind], 3, dims, strides, box1);
 }
 
-// Split factor of a launch whose segments hold `tiles` row tiles in all:
-// enough k-splits that every SM gets about one item.
-int split_for(const rwkv7_ctx *c, int tiles) {
+// Split factor of a launch whose segments hold `tiles` row tiles in all, each
+// `pairs` k-block pairs long: enough k-splits that every SM gets about one
+// item.  (Finer splits that balance several items per CTA measured slower: each
+// split adds a partial slab that the consumer reads.)  Depends only on the
+// shapes, so a slot's result does not depend on B.
+int split_for(const rwkv7_ctx *c, int tiles, int pairs) {
     const int per_sm = std::max(1, std::min(4, env_int("RWKV7_GEMM_CTAS_PER_SM", 1)));
-    int s = c->nsm * per_sm / std::max(1, tiles);
-    return std::max(1, std::min(s, MAX_SPLIT));
+    const int s = c->nsm * per_sm / std::max(1, tiles);
+    return std::max(1, std::min(s, std::min(MAX_SPLIT, pairs)));
+}
+
+// Split factors of the step's split-K projections: r, k, v + LoRA-down (s1),
+// output (s3) and channel-mix value (s5).
+void step_splits(const rwkv7_ctx *c, int *s1, int *s3, int *s5) {
+    *s1 = split_for(c, 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) + row_tiles(c, L_V1) +
+                           row_tiles(c, L_G1),
+                    kblocks(c, L_WR) / 2);
+    *s3 = split_for(c, row_tiles(c, L_WO), kblocks(c, L_WO) / 2);
+    *s5 = split_for(c, row_tiles(c, L_FV), kblocks(c, L_FV) / 2);
 }
 
 // Activation map: 2D {cols (K), bcap rows}, box {64, npad}: one copy per
@@ -356,7 +369,11 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         int stages = (int)std::min<size_t>(6, budget / stage);
         stages = std::max(2, std::min(stages, env_int("RWKV7_GEMM_STAGES", stages)));
         p.stages = stages;
-        p.accbufs = (2 * p.npad * per_sm <= 256) ? 2 : 1;
+        // Two accumulators (the next item's MMAs overlap this item's epilogue)
+        // when they fit in the 512 TMEM columns; a CTA of this kernel always
+        // has its SM to itself (its shared memory is over half of the SM's),
+        // so it may take all of them.
+        p.accbufs = (2 * p.npad * per_sm <= 512) ? 2 : 1;
         p.prefetch = nz_skip == nullptr ? 1 : 0;
         const int grid = std::min(p.nitems, c->nsm * per_sm);
         launch_gemm_tc(p, grid, gemm_tc_smem_bytes(p.npad, stages), lc, &e);
@@ -412,12 +429,8 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     pe();
     if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "embed launch: %s", cudaGetErrorString(e));
     int rc;
-    // Split factors depend only on the shapes, so a slot's result does not depend on B.
-    const int s1 = std::min(split_for(c, 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) +
-                                             row_tiles(c, L_V1) + row_tiles(c, L_G1)),
-                            kblocks(c, L_WR) / 2);
-    const int s3 = std::min(split_for(c, row_tiles(c, L_WO)), kblocks(c, L_WO) / 2);
-    const int s5 = std::min(split_for(c, row_tiles(c, L_FV)), kblocks(c, L_FV) / 2);
+    int s1, s3, s5;  // depend only on the shapes, so a slot's result does not depend on B
+    step_splits(c, &s1, &s3, &s5);
     const long long xstride = (long long)c->bcap * d;
     int px_splits = 0;  // residual partial slabs in c->px still to be added to x
     for (int l = 0; l < c->L; ++l) {
@@ -828,11 +841,8 @@ int enqueue_prefill(rwkv7_ctx *c, cudaStream_t st, int slot, int n, bool head) {
     launch_embed(ep, lc0, &e);
     if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "embed launch: %s", cudaGetErrorString(e));
     int rc;
-    const int s1 = std::min(split_for(c, 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) +
-                                             row_tiles(c, L_V1) + row_tiles(c, L_G1)),
-                            kblocks(c, L_WR) / 2);
-    const int s3 = std::min(split_for(c, row_tiles(c, L_WO)), kblocks(c, L_WO) / 2);
-    const int s5 = std::min(split_for(c, row_tiles(c, L_FV)), kblocks(c, L_FV) / 2);
+    int s1, s3, s5;
+    step_splits(c, &s1, &s3, &s5);
     const long long xstride = (long long)c->bcap * d;
     float *xa = c->x, *xb = c->x2;  // residual in, residual out of each LayerNorm phase
     int px_splits = 0;
