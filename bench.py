@@ -204,30 +204,50 @@ def run_trace_bench(args, wl):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    from recurrent_decode_gb300.prefix_cache import PrefixStateCache
     dm = synth.Dims(wl["shape"])
     weights = synth.make_weights(wl["shape"])
-    ctx = rd.Rwkv7(dm, wl["n_slots"])
+    n_cache = wl.get("cache_slots", 0)
+    ctx = rd.Rwkv7(dm, wl["n_slots"] + n_cache)
     ctx.set_weights(weights)
     del weights
     if args.mode >= 0:
         ctx.set_mode(args.mode)
     lens = synth.trace_requests(wl["n_req"], *wl["prompt_range"], *wl["out_range"])
-    reqs = []
-    for i, (pl, ol) in enumerate(lens):
-        sp = dict(temperature=wl["temperature"], top_p=wl["top_p"], top_k=wl["top_k"], presence=wl["presence"],
-                  frequency=wl["frequency"], penalty_decay=wl["penalty_decay"],
-                  seed=synth.SAMPLING_SEED_BASE + i, greedy=False)
-        reqs.append(Request(prompt=synth.prompt_tokens(dm.vocab, 1, pl, seed=10000 + i)[0], n_out=ol, sampling=sp))
+    prefix = (synth.prompt_tokens(dm.vocab, 1, wl["shared_prefix"], seed=9999)[0]
+              if wl.get("shared_prefix") else np.zeros(0, np.int32))
+
+    def make_requests():
+        reqs = []
+        for i, (pl, ol) in enumerate(lens):
+            sp = dict(temperature=wl["temperature"], top_p=wl["top_p"], top_k=wl["top_k"],
+                      presence=wl["presence"], frequency=wl["frequency"], penalty_decay=wl["penalty_decay"],
+                      seed=synth.SAMPLING_SEED_BASE + i, greedy=False)
+            tail = synth.prompt_tokens(dm.vocab, 1, pl, seed=10000 + i)[0]
+            reqs.append(Request(prompt=np.concatenate([prefix, tail]).astype(np.int32), n_out=ol, sampling=sp))
+        return reqs
+
     dev_id = None
     try:
         dev_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:
         pass
-    torch.cuda.synchronize()
-    clk = ClockSampler(dev_id)
-    stats = run_trace(ctx, reqs, wl["n_slots"], decode_prefill_ratio=wl["decode_prefill_ratio"],
-                      min_forward_seq_len=wl["min_forward_seq_len"])
-    clocks = clk.stop()
+
+    def one_run(cache):
+        for s in range(wl["n_slots"] + n_cache):
+            ctx.slot_reset(s)
+        torch.cuda.synchronize()
+        reqs = make_requests()
+        clk = ClockSampler(dev_id)
+        st = run_trace(ctx, reqs, wl["n_slots"], decode_prefill_ratio=wl["decode_prefill_ratio"],
+                       min_forward_seq_len=wl["min_forward_seq_len"], prefix_cache=cache)
+        return st, clk.stop()
+
+    uncached = None
+    if n_cache:  # the same requests without the cache first, for comparison
+        uncached, _ = one_run(None)
+    cache = PrefixStateCache(ctx, range(wl["n_slots"], wl["n_slots"] + n_cache)) if n_cache else None
+    stats, clocks = one_run(cache)
     ctx.close()
     ttft = np.array(stats.ttft_s)
     total_in = stats.prefill_tokens + stats.decode_fed_tokens + stats.generated
@@ -245,6 +265,17 @@ def run_trace_bench(args, wl):
                       "wall_s": stats.wall_s, "prefill_share": stats.prefill_tokens / max(1, total_in),
                       "ttft_s_p50": float(np.percentile(ttft, 50)), "ttft_s_p90": float(np.percentile(ttft, 90))},
             "clocks": clocks}
+    if uncached is not None:
+        ut = np.array(uncached.ttft_s)
+        line["config"]["shared_prefix"] = wl["shared_prefix"]
+        line["config"]["cache_slots"] = n_cache
+        line["prefix_cache"] = {
+            "hits": cache.hits, "misses": cache.misses, "hit_tokens": cache.hit_tokens,
+            "evictions": cache.evictions,
+            "uncached": {"value": uncached.generated / uncached.wall_s, "wall_s": uncached.wall_s,
+                         "prefill_tokens": uncached.prefill_tokens,
+                         "ttft_s_p50": float(np.percentile(ut, 50)), "ttft_s_p90": float(np.percentile(ut, 90))},
+            "note": "value / trace: the run with the cache; the same requests without it under 'uncached'"}
     if rank == 0:
         print(json.dumps(line))
     return 0

@@ -109,7 +109,10 @@ RWKV7_API int rwkv7_slot_get_state(rwkv7_ctx *ctx, int32_t slot, void *host_buf,
 RWKV7_API int rwkv7_slot_set_state(rwkv7_ctx *ctx, int32_t slot, const void *host_buf, size_t bytes);
 
 /* Consume T tokens (device int32 [T]) into one slot.  If d_logits_out is not
- * NULL it receives the fp32 logits [V] after the last token. */
+ * NULL it receives the fp32 logits [V] after the last token.  The tokens are
+ * processed in chunks of RWKV7_MAX_STEP_BATCH counted from the first one, so
+ * splitting a prompt into calls at multiples of that size gives bit-identical
+ * states (the prefix-state cache relies on this). */
 RWKV7_API int rwkv7_prefill_seq(rwkv7_ctx *ctx, int32_t slot, const int32_t *d_tokens, int32_t T,
                       float *d_logits_out);
 

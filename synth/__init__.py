@@ -54,6 +54,12 @@ WORKLOADS = {
     "trace-3pct": dict(shape="2.9b", n_slots=128, n_req=256, prompt_range=(20, 138), out_range=(1000, 3000),
                        decode_prefill_ratio=5, min_forward_seq_len=10, temperature=1.0, top_p=0.3, top_k=0,
                        presence=0.0, frequency=1.0, penalty_decay=0.996),
+    # every prompt = one shared 1024-token prefix (a system prompt) + its own
+    # tail; run with and without the prefix-state cache (8 cache slots)
+    "trace-prefix": dict(shape="2.9b", n_slots=64, n_req=128, prompt_range=(20, 138), out_range=(64, 128),
+                         shared_prefix=1024, cache_slots=8, decode_prefill_ratio=5, min_forward_seq_len=10,
+                         temperature=1.0, top_p=0.3, top_k=0, presence=0.0, frequency=1.0,
+                         penalty_decay=0.996),
 }
 
 WEIGHT_SEED = 0
