@@ -81,6 +81,9 @@ def lib():
         L.orc_layernorm.argtypes = [C.c_int, _dp, _dp, _dp, C.c_double, _dp]
         L.orc_groupnorm.argtypes = [C.c_int, C.c_int, _dp, _dp, _dp, C.c_double, _dp]
         L.orc_gemv.argtypes = [C.c_int, C.c_int, C.c_void_p, _dp, _dp]
+        L.orc_gemv_i8.argtypes = [C.c_int, C.c_int, C.c_void_p, C.c_void_p, _dp, _dp]
+        L.orc_model_set_i8.restype = C.c_int
+        L.orc_model_set_i8.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
         L.orc_f16_to_f64.restype = C.c_double
         L.orc_f16_to_f64.argtypes = [C.c_uint16]
         L.orc_f64_to_f16.restype = C.c_uint16
@@ -128,6 +131,18 @@ def gemv(W16: np.ndarray, x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
     y = np.zeros(W16.shape[0], np.float64)
     lib().orc_gemv(W16.shape[0], W16.shape[1], W16.ctypes.data, _d(x), _d(y))
+    return y
+
+
+def gemv_i8(q: np.ndarray, scale16: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """y = W x for the int8 form W[o][i] = q[o][i] * scale[o] (int8 q [rows, cols],
+    fp16 scale [rows]).  Pinned: with power-of-two scales W is exact in fp16 and
+    the result equals gemv on that fp16 matrix bit for bit."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    scale16 = np.ascontiguousarray(scale16, dtype=np.float16)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.zeros(q.shape[0], np.float64)
+    lib().orc_gemv_i8(q.shape[0], q.shape[1], q.ctypes.data, scale16.ctypes.data, _d(x), _d(y))
     return y
 
 
@@ -190,24 +205,43 @@ def exp2(e: float) -> float:
 
 # ---------------------------------------------------------------- model
 class Model:
-    """RWKV-7 model over fp16 weight arrays (dict name -> ndarray, [out, in])."""
+    """RWKV-7 model over fp16 weight arrays (dict name -> ndarray, [out, in]).
+    `int8` (optional) maps matrix names to (int8 q [out, in], fp16 scale [out]):
+    those matrices are W = q * scale per row (the int8 weight variant) and need
+    no entry in `weights`."""
 
-    def __init__(self, weights: dict, dims):
+    def __init__(self, weights: dict, dims, int8: dict | None = None):
         self.dims = dims
         self._keep = []
+        int8 = int8 or {}
         ptrs = []
         names = list(GLOBAL_ORDER)
         for l in range(dims.n_layer):
             names += [f"blocks.{l}.{n}" for n in LAYER_ORDER]
+        i8 = {}
         for n in names:
-            a = np.ascontiguousarray(weights[n], dtype=np.float16)
-            self._keep.append(a)
-            ptrs.append(a.ctypes.data)
+            if n in int8:
+                q = np.ascontiguousarray(int8[n][0], dtype=np.int8)
+                sc = np.ascontiguousarray(int8[n][1], dtype=np.float16)
+                if sc.shape != (q.shape[0],):
+                    raise ValueError(f"{n}: one fp16 scale per row expected")
+                i8[n] = (q, sc)
+                self._keep += [q, sc]
+                ptrs.append(q.ctypes.data)  # the fp16 slot is not read for an int8 matrix
+            else:
+                a = np.ascontiguousarray(weights[n], dtype=np.float16)
+                self._keep.append(a)
+                ptrs.append(a.ctypes.data)
         dd = (C.c_int32 * 9)(*dims.as_tuple())
         pp = (C.c_void_p * len(ptrs))(*ptrs)
         self.h = lib().orc_model_new(dd, pp)
         if not self.h:
             raise ValueError("oracle rejected the model dimensions")
+        for idx, n in enumerate(names):
+            if n in i8:
+                q, sc = i8[n]
+                if lib().orc_model_set_i8(self.h, idx, q.ctypes.data, sc.ctypes.data) != 0:
+                    raise ValueError(f"oracle rejected the int8 tensor {n}")
 
     def __del__(self):
         if getattr(self, "h", None) and _lib is not None:

@@ -124,6 +124,20 @@ void orc_gemv(int rows, int cols, const uint16_t *W, const double *x, double *y)
     }
 }
 
+/* The int8 weight variant: a matrix is given as int8 values q [rows][cols] and
+ * one fp16 scale per row, and stands for W[o][i] = q[o][i] * scale[o].
+ * y[o] = scale[o] * sum_i q[o][i] x[i] (the scale factored out of the row sum). */
+void orc_gemv_i8(int rows, int cols, const int8_t *q, const uint16_t *scale, const double *x, double *y) {
+    build_lut();
+#pragma omp parallel for schedule(static) if (rows >= 256)
+    for (int o = 0; o < rows; ++o) {
+        const int8_t *w = q + (size_t)o * cols;
+        double acc = 0.0;
+        for (int i = 0; i < cols; ++i) acc += (double)w[i] * x[i];
+        y[o] = H(scale[o]) * acc;
+    }
+}
+
 /* LayerNorm over n values: (x - mean) / sqrt(var + eps) * g + b, biased variance. */
 void orc_layernorm(int n, const double *x, const double *g, const double *b, double eps,
                    double *y) {
@@ -285,6 +299,8 @@ typedef struct {
     int L, d, N, H, F, V, rw, ra, rv, rg;
     const uint16_t *g[G_COUNT];
     const uint16_t **t; /* [L][T_COUNT] */
+    const int8_t **q8;      /* [G_COUNT + L * T_COUNT]: int8 values of a matrix given in int8, else NULL */
+    const uint16_t **s8;    /* its fp16 row scales */
 } orc_model;
 
 typedef struct {
@@ -306,16 +322,37 @@ orc_model *orc_model_new(const int32_t *dims, const uint16_t *const *ptrs) {
     for (int i = 0; i < G_COUNT; ++i) m->g[i] = ptrs[i];
     m->t = malloc(sizeof(uint16_t *) * (size_t)m->L * T_COUNT);
     for (int i = 0; i < m->L * T_COUNT; ++i) m->t[i] = ptrs[G_COUNT + i];
+    m->q8 = calloc((size_t)G_COUNT + (size_t)m->L * T_COUNT, sizeof(int8_t *));
+    m->s8 = calloc((size_t)G_COUNT + (size_t)m->L * T_COUNT, sizeof(uint16_t *));
     return m;
+}
+
+/* Give tensor `index` (pointer-table order) as int8 values + fp16 row scales. */
+int orc_model_set_i8(orc_model *m, int index, const int8_t *q, const uint16_t *scale) {
+    if (!m || index < 0 || index >= G_COUNT + m->L * T_COUNT || !q || !scale) return -1;
+    m->q8[index] = q;
+    m->s8[index] = scale;
+    return 0;
 }
 
 void orc_model_free(orc_model *m) {
     if (!m) return;
     free(m->t);
+    free(m->q8);
+    free(m->s8);
     free(m);
 }
 
 static inline const uint16_t *LT(const orc_model *m, int l, int k) { return m->t[l * T_COUNT + k]; }
+static inline int LI(int l, int k) { return G_COUNT + l * T_COUNT + k; }
+
+/* y = W x for matrix tensor `index`, in whichever form it was given. */
+static void mgemv(const orc_model *m, int index, int rows, int cols, const double *x, double *y) {
+    if (m->q8[index])
+        orc_gemv_i8(rows, cols, m->q8[index], m->s8[index], x, y);
+    else
+        orc_gemv(rows, cols, index < G_COUNT ? m->g[index] : m->t[index - G_COUNT], x, y);
+}
 
 static void vec16(int n, const uint16_t *p, double *out) {
     for (int i = 0; i < n; ++i) out[i] = H(p[i]);
@@ -402,34 +439,34 @@ static void tmix_front(const orc_model *m, int l, const double *x, const double 
         for (int i = 0; i < d; ++i)
             mix_out[q][i] = R16(w->xl[i] + (prev[i] - w->xl[i]) * mu[i]);
     }
-    orc_gemv(d, d, LT(m, l, T_WR), w->xr, w->r);
-    orc_gemv(d, d, LT(m, l, T_WK), w->xk, w->k);
-    orc_gemv(d, d, LT(m, l, T_WV), w->xv, w->v);
+    mgemv(m, LI(l, T_WR), d, d, w->xr, w->r);
+    mgemv(m, LI(l, T_WK), d, d, w->xk, w->k);
+    mgemv(m, LI(l, T_WV), d, d, w->xv, w->v);
     /* LoRA down projections (fp16-rounded hidden vectors) */
-    orc_gemv(m->rw, d, LT(m, l, T_W1), w->xw, w->hw);
+    mgemv(m, LI(l, T_W1), m->rw, d, w->xw, w->hw);
     for (int j = 0; j < m->rw; ++j) w->hw[j] = R16(tanh(w->hw[j]));
-    orc_gemv(m->ra, d, LT(m, l, T_A1), w->xa, w->ha);
+    mgemv(m, LI(l, T_A1), m->ra, d, w->xa, w->ha);
     for (int j = 0; j < m->ra; ++j) w->ha[j] = R16(w->ha[j]);
-    orc_gemv(m->rv, d, LT(m, l, T_V1), w->xv, w->hv);
+    mgemv(m, LI(l, T_V1), m->rv, d, w->xv, w->hv);
     for (int j = 0; j < m->rv; ++j) w->hv[j] = R16(w->hv[j]);
-    orc_gemv(m->rg, d, LT(m, l, T_G1), w->xg, w->hg);
+    mgemv(m, LI(l, T_G1), m->rg, d, w->xg, w->hg);
     for (int j = 0; j < m->rg; ++j) w->hg[j] = R16(sigm(w->hg[j]));
     /* LoRA up projections and gates */
     double *bias = w->tmp + 3 * d;
-    orc_gemv(d, m->rw, LT(m, l, T_W2), w->hw, w->dw);
+    mgemv(m, LI(l, T_W2), d, m->rw, w->hw, w->dw);
     vec16(d, LT(m, l, T_W0), bias);
     for (int i = 0; i < d; ++i) {
         w->dw[i] += bias[i];
         /* decay = exp(-exp(-0.5) * sigmoid(w0 + LoRA_w)) in (0.545, 1) */
         w->decay[i] = exp(-exp(-0.5) * sigm(w->dw[i]));
     }
-    orc_gemv(d, m->ra, LT(m, l, T_A2), w->ha, w->a);
+    mgemv(m, LI(l, T_A2), d, m->ra, w->ha, w->a);
     vec16(d, LT(m, l, T_A0), bias);
     for (int i = 0; i < d; ++i) w->a[i] = sigm(bias[i] + w->a[i]);
-    orc_gemv(d, m->rv, LT(m, l, T_V2), w->hv, w->vg);
+    mgemv(m, LI(l, T_V2), d, m->rv, w->hv, w->vg);
     vec16(d, LT(m, l, T_V0), bias);
     for (int i = 0; i < d; ++i) w->vg[i] = sigm(bias[i] + w->vg[i]);
-    orc_gemv(d, m->rg, LT(m, l, T_G2), w->hg, w->g);
+    mgemv(m, LI(l, T_G2), d, m->rg, w->hg, w->g);
     /* removal key kh = normalize(k * k_k) per head; modified key kp = k * (1 + (a-1) k_a) */
     double *kk = w->tmp, *ka = w->tmp + d;
     vec16(d, LT(m, l, T_KK), kk);
@@ -468,7 +505,7 @@ static void tmix_back(const orc_model *m, int l, double *x, orc_tok *w) {
         for (int i = 0; i < N; ++i) w->z[h * N + i] += bonus * w->vp[h * N + i];
     }
     for (int i = 0; i < d; ++i) w->z[i] = R16(w->z[i] * w->g[i]);
-    orc_gemv(d, d, LT(m, l, T_WO), w->z, o);
+    mgemv(m, LI(l, T_WO), d, d, w->z, o);
     for (int i = 0; i < d; ++i) x[i] += o[i];
 }
 
@@ -484,12 +521,12 @@ static void cmix(const orc_model *m, int l, double *x, const double *prev, doubl
     vec16(d, LT(m, l, T_FXK), mu);
     for (int i = 0; i < d; ++i) xk[i] = R16(xl2_out[i] + (prev[i] - xl2_out[i]) * mu[i]);
     double *hbuf = malloc(sizeof(double) * F), *o = malloc(sizeof(double) * d);
-    orc_gemv(F, d, LT(m, l, T_FK), xk, hbuf);
+    mgemv(m, LI(l, T_FK), F, d, xk, hbuf);
     for (int f = 0; f < F; ++f) {
         double t = hbuf[f] > 0.0 ? hbuf[f] : 0.0;
         hbuf[f] = R16(t * t);
     }
-    orc_gemv(d, F, LT(m, l, T_FV), hbuf, o);
+    mgemv(m, LI(l, T_FV), d, F, hbuf, o);
     for (int i = 0; i < d; ++i) x[i] += o[i];
     free(hbuf);
     free(o);
@@ -512,7 +549,7 @@ static void head(const orc_model *m, const double *x, double *logits, double *tm
     vec16(d, m->g[G_LNOB], bet);
     orc_layernorm(d, x, gam, bet, 1e-5, xo);
     for (int i = 0; i < d; ++i) xo[i] = R16(xo[i]);
-    orc_gemv(m->V, d, m->g[G_HEAD], xo, logits);
+    mgemv(m, G_HEAD, m->V, d, xo, logits);
 }
 
 /*

@@ -186,6 +186,72 @@ def make_weights(shape: str, seed: int = WEIGHT_SEED, threads: int | None = None
     return out
 
 
+# The int8 weight variant: these matrices are given as int8 values with one
+# fp16 scale per output row (W = q * scale); everything else stays fp16.
+I8_LAYER_MATRICES = ("att.w1", "att.w2", "att.a1", "att.a2", "att.v1", "att.v2", "att.g1", "att.g2",
+                     "att.receptance", "att.key", "att.value", "att.output", "ffn.key", "ffn.value")
+I8_Q_STD = float(np.sqrt((255.0 ** 2 - 1.0) / 12.0))  # std of q uniform on [-127, 127]
+
+
+def i8_matrix_names(dims: Dims):
+    return [f"blocks.{l}.{m}" for l in range(dims.n_layer) for m in I8_LAYER_MATRICES] + ["head"]
+
+
+def _fill_i8(q: np.ndarray, seed: int, tid: int, c0: int, c1: int):
+    flat = q.reshape(-1)
+    for c in range(c0, c1):
+        lo = c * _CHUNK
+        hi = min(flat.size, lo + _CHUNK)
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tid, c, 8])))
+        flat[lo:hi] = g.integers(-127, 128, size=hi - lo, dtype=np.int8)
+
+
+def make_weights_i8(shape: str, seed: int = WEIGHT_SEED, threads: int | None = None,
+                    n_layer: int | None = None, pow2_scales: bool = False):
+    """Weights of the int8 variant for the named shape: ({name: fp16 ndarray} for
+    every tensor that is not an int8 matrix -- the same values make_weights draws
+    -- , {name: (int8 q [out, in], fp16 scale [out])}).  q is uniform on
+    [-127, 127]; a row's scale is 0.02 / I8_Q_STD * U(0.75, 1.25), so the matrix
+    has about the fp16 variant's N(0, 0.02) spread; with pow2_scales every scale
+    is 2^-12 or 2^-13 instead (q * scale is then exact in fp16)."""
+    dims = Dims(shape, n_layer)
+    specs = tensor_specs(dims)
+    i8set = set(i8_matrix_names(dims))
+    out = {name: np.empty(shp, dtype=np.float16) for name, shp, _ in specs if name not in i8set}
+    q8 = {name: np.empty(shp, dtype=np.int8) for name, shp, _ in specs if name in i8set}
+    jobs = []
+    for tid, (name, shp, init) in enumerate(specs):
+        nchunks = (int(np.prod(shp)) + _CHUNK - 1) // _CHUNK
+        for c0 in range(0, nchunks, 4):
+            jobs.append((name, init, tid, c0, min(nchunks, c0 + 4)))
+
+    def run(j):
+        name, init, tid, c0, c1 = j
+        if name in i8set:
+            _fill_i8(q8[name], seed, tid, c0, c1)
+        else:
+            _fill(out[name], init, seed, tid, c0, c1)
+
+    nthr = threads or min(32, os.cpu_count() or 1)
+    if nthr <= 1 or len(jobs) < 8:
+        for j in jobs:
+            run(j)
+    else:
+        with ThreadPoolExecutor(nthr) as ex:
+            list(ex.map(run, jobs))
+    int8 = {}
+    for tid, (name, shp, _) in enumerate(specs):
+        if name not in i8set:
+            continue
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tid, 9])))
+        if pow2_scales:
+            sc = np.where(g.random(shp[0]) < 0.5, 2.0 ** -12, 2.0 ** -13)
+        else:
+            sc = 0.02 / I8_Q_STD * (0.75 + 0.5 * g.random(shp[0]))
+        int8[name] = (q8[name], sc.astype(np.float16))
+    return out, int8
+
+
 def prompt_tokens(vocab: int, n_seq: int, length: int, seed: int = PROMPT_SEED):
     """Uniform random token ids, one independent stream per sequence: int32 [n_seq, length]."""
     rows = []
@@ -257,4 +323,5 @@ def read_weight_file(path: str):
 
 __all__ = ["SHAPES", "WORKLOADS", "Dims", "tensor_specs", "n_params", "make_weights",
            "prompt_tokens", "random_logits", "trace_requests", "write_weight_file",
+           "make_weights_i8", "i8_matrix_names", "I8_LAYER_MATRICES",
            "read_weight_file"]
