@@ -79,6 +79,20 @@ typedef struct {
  * scratch.  cuda_stream: a cudaStream_t (may be NULL). */
 RWKV7_API int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out);
 
+/* As rwkv7_create, with the weight format of the projection matrices:
+ * weight_bits 16 (fp16, as rwkv7_create) or 8 -- the int8 weight variant, in
+ * which every matrix the step streams (r, k, v, output, LoRA, channel-mix key
+ * and value, head; not the embedding) is int8 values q [out, in] with one fp16
+ * scale per output row, W = q * scale, set with rwkv7_set_weight_i8; the other
+ * tensors stay fp16.  The roadmap of the RWKV-Runner Albatross article lists
+ * int8 weights among the engine's next steps; the scale per row is this
+ * library's choice.  An int8 context runs the tensor-core modes 0 and 1 only.
+ * Returns RWKV7_EINVAL for another weight_bits. */
+RWKV7_API int rwkv7_create_ex(const rwkv7_config *cfg, int32_t weight_bits, void *cuda_stream, rwkv7_ctx **out);
+
+/* 16 or 8 (see rwkv7_create_ex); 0 for NULL. */
+RWKV7_API int32_t rwkv7_weight_bits(const rwkv7_ctx *ctx);
+
 /* Free everything the ctx owns (synchronizes its stream first).  NULL is a no-op. */
 RWKV7_API void rwkv7_destroy(rwkv7_ctx *ctx);
 
@@ -89,6 +103,14 @@ RWKV7_API const char *rwkv7_last_error(const rwkv7_ctx *ctx);
  * "blocks.3.att.key" [d, d], "blocks.3.ffn.value" [d, d_ffn]).  bytes must be
  * the tensor's exact size.  Synchronous. */
 RWKV7_API int rwkv7_set_weight(rwkv7_ctx *ctx, const char *name, const void *host_f16, size_t bytes);
+
+/* Int8 context only: copy one named matrix given as host int8 values q
+ * [out][in] (q_bytes = out * in) and fp16 row scales [out] (scale_bytes =
+ * 2 * out).  RWKV7_ESHAPE for a name that is not an int8 matrix of this
+ * context or for wrong sizes; rwkv7_set_weight refuses these names in an int8
+ * context.  Synchronous. */
+RWKV7_API int rwkv7_set_weight_i8(rwkv7_ctx *ctx, const char *name, const int8_t *host_q, size_t q_bytes,
+                                  const void *host_scale_f16, size_t scale_bytes);
 
 /* Read every tensor from an RWKV7W01 weight file (text header, 256-byte aligned
  * fp16 data) and set it.  Synchronous. */

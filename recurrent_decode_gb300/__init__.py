@@ -43,6 +43,9 @@ class Sampling(C.Structure):
 _VP, _I32P, _FP = C.c_void_p, C.POINTER(C.c_int32), C.c_void_p
 SIGNATURES = {
     "rwkv7_create": (C.c_int, [C.POINTER(Config), C.c_void_p, C.POINTER(C.c_void_p)]),
+    "rwkv7_create_ex": (C.c_int, [C.POINTER(Config), C.c_int32, C.c_void_p, C.POINTER(C.c_void_p)]),
+    "rwkv7_weight_bits": (C.c_int32, [_VP]),
+    "rwkv7_set_weight_i8": (C.c_int, [_VP, C.c_char_p, C.c_void_p, C.c_size_t, C.c_void_p, C.c_size_t]),
     "rwkv7_destroy": (None, [_VP]),
     "rwkv7_last_error": (C.c_char_p, [_VP]),
     "rwkv7_set_weight": (C.c_int, [_VP, C.c_char_p, C.c_void_p, C.c_size_t]),
@@ -150,9 +153,11 @@ def sample_rows_static(logits, rows, occ, params, ndraw, next_out, err, stream=N
 class Rwkv7:
     """One library context: device weights + a pool of n_slots state slots."""
 
-    def __init__(self, dims, n_slots: int, stream=None):
+    def __init__(self, dims, n_slots: int, stream=None, weight_bits: int = 16):
         """dims: object with n_layer, d_model, head_size, d_ffn, vocab, lora_w/a/v/g
-        (e.g. synth.Dims).  stream: torch.cuda.Stream or None (current stream)."""
+        (e.g. synth.Dims).  stream: torch.cuda.Stream or None (current stream).
+        weight_bits: 16 (fp16 matrices) or 8 (int8 matrices with fp16 row scales,
+        rwkv7_create_ex)."""
         import torch
         self.lib = load_library()
         self.dims = dims
@@ -161,7 +166,9 @@ class Rwkv7:
         cfg = Config(dims.n_layer, dims.d_model, dims.head_size, dims.d_ffn, dims.vocab,
                      dims.lora_w, dims.lora_a, dims.lora_v, dims.lora_g, self.n_slots)
         h = C.c_void_p()
-        rc = self.lib.rwkv7_create(C.byref(cfg), C.c_void_p(self.stream.cuda_stream), C.byref(h))
+        self.weight_bits = int(weight_bits)
+        rc = self.lib.rwkv7_create_ex(C.byref(cfg), self.weight_bits, C.c_void_p(self.stream.cuda_stream),
+                                      C.byref(h))
         self.h = h
         if rc != OK:
             msg = self.lib.rwkv7_last_error(h).decode() if h.value else "invalid configuration"
@@ -190,9 +197,19 @@ class Rwkv7:
         a = np.ascontiguousarray(arr, dtype=np.float16)
         self._check(self.lib.rwkv7_set_weight(self.h, name.encode(), a.ctypes.data, a.nbytes))
 
-    def set_weights(self, weights: dict):
+    def set_weights(self, weights: dict, int8: dict | None = None):
+        """weights: {name: fp16 array}; int8 (int8 context): {name: (int8 q [out, in],
+        fp16 scale [out])} for the int8 matrices."""
         for n, a in weights.items():
             self.set_weight(n, a)
+        for n, (q, sc) in (int8 or {}).items():
+            self.set_weight_i8(n, q, sc)
+
+    def set_weight_i8(self, name: str, q: np.ndarray, scale: np.ndarray):
+        q = np.ascontiguousarray(q, dtype=np.int8)
+        sc = np.ascontiguousarray(scale, dtype=np.float16)
+        self._check(self.lib.rwkv7_set_weight_i8(self.h, name.encode(), q.ctypes.data, q.nbytes,
+                                                  sc.ctypes.data, sc.nbytes))
 
     def load_weights(self, path: str):
         self._check(self.lib.rwkv7_load_weights(self.h, os.fsencode(path)))

@@ -92,6 +92,8 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
     const bool live = n < sg.rows;
     float bias = 0.0f;
     if ((KIND == EPI_DECAY || KIND == EPI_SIGMOID_BIAS) && live) bias = __half2float(sg.bias[n]);
+    const bool scaled = sg.wscale != nullptr;  // int8 weights: the row sum times the row's scale
+    const float wsc = scaled && live ? __half2float(sg.wscale[n]) : 1.0f;
     bool nz = false;
     for (int cb = c0; cb < npad; cb += EPI_GROUPS * EPI_CW) {
         float v[EPI_CW];
@@ -102,6 +104,10 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
             for (int q = 0; q < EPI_CW; ++q) v[q] = 0.0f;
         }
         if (!live) continue;
+        if (scaled) {
+#pragma unroll
+            for (int q = 0; q < EPI_CW; ++q) v[q] *= wsc;
+        }
         const int nq = min(EPI_CW, B - cb);
         if (KIND == -1) {  // raw fp32 partial
             float *out = (float *)sg.out + (size_t)split * sg.split_stride + (size_t)cb * sg.ldo + n;
@@ -432,6 +438,385 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
     }
+}
+
+// ---------------------------------------------------------------------------
+// int8-weight variant.  A weight tile arrives as 128 rows x 64 int8 (8 KB; the
+// int8 tiles keep the fp16 tile order) and is widened to fp16 in shared memory
+// before tcgen05.mma kind::f16 reads it; the row scale multiplies the finished
+// sum in the epilogue (W = q * scale per row, so W x = scale * (q x)).
+// Two rings: ring A holds, per stage, the int8 tiles of kbs k-blocks and the
+// activation boxes; ring B the converted fp16 tiles in the SW128 K-major layout
+// the TMA would have produced (16-byte chunk c of row r at chunk c ^ (r & 7)).
+// Roles: warp 0 lane 0 loads ring A (the int8 tiles of the first stages before
+// the dependency wait); warp 1 lane 0 issues the MMAs; the 16 epilogue warps
+// convert ring A's int8 tiles into ring B while the mainloop runs and run the
+// epilogue after each item.  Barriers: full_w / full_x (int8 / activation bytes
+// of a ring A stage landed), empty_a (16 converter warps + the MMA commit),
+// full_b (16 converter warps), empty_b (the MMA commit).
+// ---------------------------------------------------------------------------
+constexpr uint32_t W8_TILE_BYTES = GEMM_TILE_M * GEMM_TILE_K;  // 8 KB
+
+// 16 int8 (one 16-byte chunk) -> 16 fp16 at two swizzled 16-byte chunks.  Exact:
+// the byte x ^ 0x80 = x + 128 is placed in the low mantissa byte of the fp16
+// 1024.0 (0x6400), giving 1024 + 128 + x, and 1152 is subtracted.
+__device__ __forceinline__ void widen16(const uint8_t *src, uint8_t *dst_row, int g, int r) {
+    const uint4 in = *reinterpret_cast<const uint4 *>(src);
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t o[8];
+    const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6480u),
+                                       __ushort_as_half((unsigned short)0x6480u));  // 1152
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t u = w[k] ^ 0x80808080u;
+        const uint32_t lo = __byte_perm(u, 0x64646464u, 0x5140u);
+        const uint32_t hi = __byte_perm(u, 0x64646464u, 0x5342u);
+        __half2 hl = __hsub2(*reinterpret_cast<const __half2 *>(&lo), off);
+        __half2 hh = __hsub2(*reinterpret_cast<const __half2 *>(&hi), off);
+        o[2 * k] = *reinterpret_cast<uint32_t *>(&hl);
+        o[2 * k + 1] = *reinterpret_cast<uint32_t *>(&hh);
+    }
+    const int c0 = 2 * g, c1 = 2 * g + 1, sw = r & 7;
+    *reinterpret_cast<uint4 *>(dst_row + ((c0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(dst_row + ((c1 ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__device__ __forceinline__ bool stage_skipped_k(const uint32_t *flags, int kb, int kbs) {
+    return flags != nullptr && flags[kb] == 0u && (kbs == 1 || flags[kb + 1] == 0u);
+}
+
+__global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ GemmSeg sseg[GEMM_MAX_SEG];
+    __shared__ uint32_t snz[MAX_NZ_BLOCKS];
+    __shared__ uint64_t flags_ready;
+    __shared__ uint32_t s_ok;
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int SA = p.stages, SB = p.stages_b, KBS = p.kbs;
+    const int B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, nitems = p.nitems;
+    const bool has_skip = p.nz_skip != nullptr;
+    const uint32_t *skip = has_skip ? snz : nullptr;
+    const uint32_t XKB = (uint32_t)npad * 128u;        // one activation k-block
+    const uint32_t W8B = (uint32_t)KBS * W8_TILE_BYTES;  // int8 tiles of a stage
+    const uint32_t XB = (uint32_t)KBS * XKB;            // activations of a stage
+    const uint32_t AB = W8B + XB;                       // ring A stage (a multiple of 1024)
+    const uint32_t W16B = (uint32_t)KBS * W_TILE_BYTES; // ring B stage
+    uint8_t *sA = base;
+    uint8_t *sB = base + (size_t)SA * AB;
+    uint64_t *full_w = (uint64_t *)(sB + (size_t)SB * W16B);
+    uint64_t *full_x = full_w + SA;
+    uint64_t *empty_a = full_x + SA;
+    uint64_t *full_b = empty_a + SA;
+    uint64_t *empty_b = full_b + SB;
+    uint64_t *acc_full = empty_b + SB;   // [2]
+    uint64_t *acc_empty = acc_full + 2;  // [2]
+    uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+    uint32_t *nzf = tmem_slot + 2;  // [2]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int i_begin = item_first(c, G, nitems), i_end = item_first(c + 1, G, nitems);
+    uint32_t ncols = 32;
+    while ((int)ncols < NB * npad) ncols <<= 1;
+
+    if (threadIdx.x < nseg) sseg[threadIdx.x] = p.seg[threadIdx.x];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < SA; ++i) {
+            mbar_init(&full_w[i], 1);
+            mbar_init(&full_x[i], 1);
+            mbar_init(&empty_a[i], EPI_WARPS + 1);
+        }
+        for (int i = 0; i < SB; ++i) {
+            mbar_init(&full_b[i], EPI_WARPS);
+            mbar_init(&empty_b[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], EPI_THREADS);
+        }
+        mbar_init(&flags_ready, 1);
+        *abort_flag = 0u;
+        nzf[0] = nzf[1] = 0u;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // int8 tiles of the first stages before the dependency wait (weights are constant)
+    int npre = 0;
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.maps[i]);
+        if (p.prefetch) {
+            const uint64_t polW = policy_evict_first();
+            for (int i = i_begin; i < i_end && npre < SA; ++i) {
+                const Item it = locate_item(sseg, nseg, i);
+                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
+                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
+                for (int kb = it.kb0; kb < it.kb1 && npre < SA; kb += KBS, ++npre) {
+                    mbar_expect_tx(&full_w[npre], W8B);
+                    tma_load_3d(sA + (size_t)npre * AB, wm, &full_w[npre], 0, 0, tb + kb, polW);
+                }
+            }
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (ring A)
+        if (lane == 0) {
+            const uint64_t polW = policy_evict_first(), polX = policy_evict_last();
+            pdl_wait();
+            pdl_launch();
+            bool ok = true;
+            if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
+            int q = 0;
+            for (int i = i_begin; i < i_end && ok; ++i) {
+                const Item it = locate_item(sseg, nseg, i);
+                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
+                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
+                const CUtensorMap *xm = &p.maps[sseg[it.s].xmap];
+                for (int kb = it.kb0; kb < it.kb1; kb += KBS) {
+                    if (stage_skipped_k(skip, kb, KBS)) continue;
+                    const int st = q % SA;
+                    uint8_t *sa = sA + (size_t)st * AB;
+                    if (q >= npre) {
+                        if (q >= SA && !mbar_wait(&empty_a[st], (uint32_t)((q / SA) - 1) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(&full_w[st], W8B);
+                        tma_load_3d(sa, wm, &full_w[st], 0, 0, tb + kb, polW);
+                    }
+                    mbar_expect_tx(&full_x[st], XB);
+                    if (sseg[it.s].x3) {
+                        tma_load_3d(sa + W8B, xm, &full_x[st], 0, 0, kb, polX);
+                    } else {
+                        for (int h = 0; h < KBS; ++h)
+                            tma_load_2d(sa + W8B + (size_t)h * XKB, xm, &full_x[st], (kb + h) * GEMM_TILE_K, 0, polX);
+                    }
+                    ++q;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1u;
+                atomicOr(p.err, ERR_TIMEOUT);
+            }
+            // Before leaving, wait (bounded) until no copy issued here is in flight:
+            // int8 tiles of stages < max(q, npre) (prefetched ones may be ahead of
+            // q after an abort), activations of stages < q.
+            const int qw = q > npre ? q : npre;
+            for (int j = (qw > SA ? qw - SA : 0); j < qw; ++j)
+                if (!mbar_wait_any(&full_w[j % SA], (uint32_t)(j / SA) & 1u)) break;
+            for (int j = (q > SA ? q - SA : 0); j < q; ++j)
+                if (!mbar_wait_any(&full_x[j % SA], (uint32_t)(j / SA) & 1u)) break;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(GEMM_TILE_M, npad);
+            bool ok = true;
+            if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
+            int q = 0, n = 0;
+            for (int i = i_begin; i < i_end && ok; ++i, ++n) {
+                const Item it = locate_item(sseg, nseg, i);
+                const int buf = n % NB;
+                if (n >= NB && !mbar_wait(&acc_empty[buf], (uint32_t)((n / NB) - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * npad);
+                uint32_t issued = 0;
+                for (int kb = it.kb0; kb < it.kb1; kb += KBS) {
+                    if (stage_skipped_k(skip, kb, KBS)) continue;
+                    const int sa = q % SA, sb = q % SB;
+                    if (!mbar_wait(&full_x[sa], (uint32_t)(q / SA) & 1u, abort_flag) ||
+                        !mbar_wait(&full_b[sb], (uint32_t)(q / SB) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sB + (size_t)sb * W16B);
+                    const uint32_t b0 = smem_u32(sA + (size_t)sa * AB + W8B);
+                    for (int h = 0; h < KBS; ++h) {
+#pragma unroll
+                        for (int kk = 0; kk < GEMM_TILE_K / 16; ++kk)
+                            mma_f16(d_tmem, sdesc_k128(a0 + h * W_TILE_BYTES + kk * 32),
+                                    sdesc_k128(b0 + h * XKB + kk * 32), idesc,
+                                    (issued | (uint32_t)h | (uint32_t)kk) ? 1u : 0u);
+                    }
+                    issued = 1;
+                    mma_commit(&empty_a[sa]);
+                    mma_commit(&empty_b[sb]);
+                    ++q;
+                }
+                if (!ok) break;
+                if (issued)
+                    mma_commit(&acc_full[buf]);
+                else
+                    mbar_arrive(&acc_full[buf]);
+            }
+            if (!ok) {
+                *abort_flag = 1u;
+                atomicOr(p.err, ERR_TIMEOUT);
+            }
+        }
+    } else {
+        // ------------------------------------------------ converters + epilogue
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const int et = threadIdx.x - 64;
+        const int grp = et >> 7;
+        uint32_t *nz_out = p.nz_out;
+        bool waited = false;
+        if (has_skip) {
+            pdl_wait();
+            waited = true;
+            const int nkb = sseg[0].kb < MAX_NZ_BLOCKS ? sseg[0].kb : MAX_NZ_BLOCKS;
+            const int nreal = (sseg[0].K + GEMM_TILE_K - 1) / GEMM_TILE_K;
+            for (int j = et; j < nkb; j += EPI_THREADS) snz[j] = j < nreal ? p.nz_skip[j] : 0u;
+            named_bar(1, EPI_THREADS);
+            if (et == 0) mbar_arrive(&flags_ready);
+        }
+        int q = 0, n = 0;
+        bool ok = true, dead = false;
+        for (int i = i_begin; i < i_end && ok; ++i, ++n) {
+            const Item it = locate_item(sseg, nseg, i);
+            const GemmSeg sg = sseg[it.s];
+            const int buf = n % NB;
+            bool valid = false;
+            // convert this item's stages (each thread: KBS 16-byte int8 chunks per stage)
+            for (int kb = it.kb0; kb < it.kb1; kb += KBS) {
+                if (stage_skipped_k(skip, kb, KBS)) continue;
+                valid = true;
+                const int sa = q % SA, sb = q % SB;
+                ++q;
+                if (dead) continue;  // an earlier wait gave up: convert nothing more
+                uint32_t w_ok = 0u;
+                if (lane == 0) {
+                    bool okw = mbar_wait(&full_w[sa], (uint32_t)((q - 1) / SA) & 1u, abort_flag);
+                    if (okw && q - 1 >= SB)
+                        okw = mbar_wait(&empty_b[sb], (uint32_t)(((q - 1) / SB) - 1) & 1u, abort_flag);
+                    if (!okw) {
+                        *abort_flag = 1u;
+                        atomicOr(p.err, ERR_TIMEOUT);
+                    }
+                    w_ok = okw ? 1u : 0u;
+                }
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (!w_ok) {
+                    dead = true;
+                    continue;
+                }
+                // acquire the landed int8 bytes / the released fp16 stage in every lane
+                (void)mbar_try_wait(&full_w[sa], (uint32_t)((q - 1) / SA) & 1u);
+                if (q - 1 >= SB) (void)mbar_try_wait(&empty_b[sb], (uint32_t)(((q - 1) / SB) - 1) & 1u);
+                const uint8_t *a8 = sA + (size_t)sa * AB;
+                uint8_t *b16 = sB + (size_t)sb * W16B;
+                for (int u = et; u < KBS * 512; u += EPI_THREADS) {
+                    const int h = u >> 9, r = (u >> 2) & 127, g = u & 3;
+                    widen16(a8 + (size_t)h * W8_TILE_BYTES + r * 64 + g * 16,
+                            b16 + (size_t)h * W_TILE_BYTES + r * 128, g, r);
+                }
+                fence_proxy_async();  // generic-proxy writes -> visible to the tensor cores
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&full_b[sb]);
+                    mbar_arrive(&empty_a[sa]);
+                }
+            }
+            if (!waited) {  // outputs may be read by the preceding kernel until it completes
+                pdl_wait();
+                waited = true;
+            }
+            // epilogue of the item (as in gemm_tc_kernel); thread 0 decides for all
+            // 512 threads, so that they take the same path through the named barriers
+            named_bar(3, EPI_THREADS);
+            if (et == 0)
+                s_ok = (!*abort_flag && mbar_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u, abort_flag)) ? 1u : 0u;
+            named_bar(3, EPI_THREADS);
+            const bool ok_wait = s_ok != 0u;
+            named_bar(3, EPI_THREADS);
+            if (!ok_wait) {
+                ok = false;
+                break;
+            }
+            (void)mbar_try_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u);
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
+            const int nrow = it.tile * GEMM_TILE_M + row;
+            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B, grp * EPI_CW);
+            tc_fence_before();
+            mbar_arrive(&acc_empty[buf]);
+            if (sg.epi == EPI_RELU2 && sg.S == 1 && nz_out != nullptr) {
+                const unsigned bal = __ballot_sync(0xffffffffu, nzany);
+                if (lane == 0 && bal) atomicOr(&nzf[qd >> 1], 1u);
+                named_bar(2, EPI_THREADS);
+                if (et == 0) {
+                    const int blk0 = it.tile * 2;
+                    const int nblk = (sg.rows + 63) / 64;
+                    const uint32_t f0 = ((volatile uint32_t *)nzf)[0], f1 = ((volatile uint32_t *)nzf)[1];
+                    nzf[0] = nzf[1] = 0u;
+                    if (blk0 < nblk) nz_out[blk0] = f0;
+                    if (blk0 + 1 < nblk) nz_out[blk0 + 1] = f1;
+                    const unsigned long long nnz = (blk0 < nblk ? f0 : 0u) + (blk0 + 1 < nblk ? f1 : 0u);
+                    if (p.nz_count && nnz) atomicAdd(p.nz_count, nnz);
+                }
+                named_bar(2, EPI_THREADS);
+            }
+        }
+        if (!ok && et == 0) {
+            *abort_flag = 1u;
+            atomicOr(p.err, ERR_TIMEOUT);
+        }
+        if (!waited) pdl_wait();
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, ncols);
+    }
+}
+
+size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a, int stages_b) {
+    const size_t ab = (size_t)kbs * (W8_TILE_BYTES + (size_t)npad * 128);
+    const size_t bb = (size_t)kbs * W_TILE_BYTES;
+    return 1024 + (size_t)stages_a * ab + (size_t)stages_b * bb + (size_t)(3 * stages_a + 2 * stages_b + 4) * 8 + 64;
+}
+
+void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t r = cudaFuncSetAttribute(gemm_tc8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             gemm_tc_max_smem());
+        if (r != cudaSuccess) {
+            *e = r;
+            return;
+        }
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(GEMM_TC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = lc.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = lc.pdl ? 1 : 0;
+    cudaError_t r = cudaLaunchKernelEx(&cfg, gemm_tc8_kernel, p);
+    if (r != cudaSuccess) *e = r;
 }
 
 size_t gemm_tc_smem_bytes(int npad, int stages) {

@@ -60,6 +60,7 @@ struct GemmSeg {
     int ldo;              // out element index = b * ldo + n (+ j * split_stride)
     long long split_stride;
     const __half *bias;   // [rows] (EPI_DECAY / EPI_SIGMOID_BIAS)
+    const __half *wscale; // int8 weights: fp16 scale per output row (applied to the sum), else null
     const __half *w;      // tiled weights of this layer (SIMT path)
     const __half *x;      // activations [B][ldx] (SIMT path)
     int ldx;
@@ -70,7 +71,9 @@ struct GemmParams {
     GemmSeg seg[GEMM_MAX_SEG];
     int nseg, nmaps, nitems;
     int B, npad;                     // slots in the step, MMA N (B rounded up to 16)
-    int stages;                      // smem pipeline depth
+    int stages;                      // smem pipeline depth (int8 weights: stages of the int8 + activation ring)
+    int stages_b;                    // int8 weights: stages of the converted fp16 weight ring
+    int kbs;                         // int8 weights: k-blocks per stage (1 or 2); fp16 weights: always 2
     int accbufs;                     // TMEM accumulator buffers (1 or 2)
     int prefetch;                    // 1: weights may be fetched before the dependency wait
     uint32_t *nz_out;                // EPI_RELU2: flag per 64 output rows
@@ -88,6 +91,10 @@ struct LaunchCfg {
 void launch_gemm_tc(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e);
 void launch_gemm_simt(const GemmParams &p, const LaunchCfg &lc, cudaError_t *e);
 size_t gemm_tc_smem_bytes(int npad, int stages);
+// int8-weight GEMM: weights arrive as int8 tiles and are converted to fp16 in
+// shared memory by the epilogue warps before the tensor cores read them.
+void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e);
+size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a, int stages_b);
 size_t gemm_tc_stage_bytes(int npad);
 int gemm_tc_max_smem();
 
@@ -320,6 +327,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Bounded wait that ignores the abort word: used to drain copies still in
+// flight before a CTA exits, when the abort word may already be set.
+__device__ __forceinline__ bool mbar_wait_any(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && gtimer() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

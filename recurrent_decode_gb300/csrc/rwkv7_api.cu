@@ -92,6 +92,11 @@ struct rwkv7_ctx {
     int wrows[W_COUNT]{}, wcols[W_COUNT]{};
     bool tiled[W_COUNT]{};
     __half *w[W_COUNT]{};
+    // int8 weight variant (wbits == 8): the tiled matrices as int8 tiles
+    // [layer][row tile][k-block][128][64] and fp16 row scales [layer][tiles * 128]
+    int wbits = 16;
+    int8_t *w8[W_COUNT]{};
+    __half *wsc[W_COUNT]{};
     std::vector<uint8_t> wset;  // [W_COUNT][L] (globals use index 0)
     size_t n_missing = 0;
 
@@ -120,6 +125,8 @@ struct rwkv7_ctx {
 
     CUtensorMap wmap[W_COUNT]{};
     CUtensorMap wmap1[W_COUNT]{};  // box of one k-block tile (persistent step with N > 128)
+    CUtensorMap wmap8[W_COUNT]{};  // int8 tiles, two k-blocks per copy
+    CUtensorMap wmap8_1[W_COUNT]{};  // int8 tiles, one k-block per copy
     bool has_wmap[W_COUNT]{};
     CUtensorMap amap[A_COUNT][MAX_B / 16]{};
     bool amap_ok[A_COUNT][MAX_B / 16]{};
@@ -179,7 +186,7 @@ int env_int(const char *name, int dflt) {
 }
 
 int make_map(rwkv7_ctx *c, CUtensorMap *m, void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
-             const uint32_t *box) {
+             const uint32_t *box, bool int8 = false) {
     auto fn = encode_fn();
     if (!fn) return fail(c, RWKV7_ECUDA, "cuTensorMapEncodeTiled is not available");
     cuuint64_t gd[3], gs[2];
@@ -189,8 +196,11 @@ int make_map(rwkv7_ctx *c, CUtensorMap *m, void *base, int rank, const uint64_t 
         bx[i] = box[i];
     }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, base, gd, gs, bx, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    // fp16 tiles land in the SW128 K-major layout the tensor cores read; int8
+    // tiles land row-major (64 bytes a row) and are widened by the kernel
+    CUresult r = fn(m, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank,
+                    base, gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(c, RWKV7_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return RWKV7_OK;
@@ -210,6 +220,15 @@ size_t layer_elems(const rwkv7_ctx *c, int kind) {
 int make_wmap(rwkv7_ctx *c, int kind) {
     const int layers = per_layer(kind) ? c->L : 1;
     const uint64_t ntiles = (uint64_t)layers * row_tiles(c, kind) * kblocks(c, kind);
+    if (c->wbits == 8) {  // 8 KB int8 tiles, 64-byte rows
+        uint64_t dims8[3] = {(uint64_t)GEMM_TILE_K, (uint64_t)GEMM_TILE_M, ntiles};
+        uint64_t strides8[2] = {(uint64_t)GEMM_TILE_K, (uint64_t)GEMM_TILE_K * GEMM_TILE_M};
+        uint32_t box2[3] = {64, 128, 2}, box1[3] = {64, 128, 1};
+        c->has_wmap[kind] = true;
+        int rc = make_map(c, &c->wmap8[kind], c->w8[kind], 3, dims8, strides8, box2, true);
+        if (rc) return rc;
+        return make_map(c, &c->wmap8_1[kind], c->w8[kind], 3, dims8, strides8, box1, true);
+    }
     uint64_t dims[3] = {(uint64_t)GEMM_TILE_K, (uint64_t)GEMM_TILE_M, ntiles};
     uint64_t strides[2] = {(uint64_t)GEMM_TILE_K * 2, (uint64_t)GEMM_TILE_K * GEMM_TILE_M * 2};
     uint32_t box[3] = {64, 128, 2};
@@ -302,6 +321,10 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
     for (int i = 0; i < W_COUNT; ++i) wslot[i] = -1;
     for (int i = 0; i < A_COUNT; ++i) aslot[i] = -1;
     int item = 0, blk = 0;
+    const bool w8 = c->wbits == 8;
+    // int8 weights: k-blocks per ring stage -- pairs while the activation boxes
+    // are small, single k-blocks for wide batches (so that four stages fit)
+    const int kbs8 = (B + 15) / 16 * 16 > 128 ? 1 : 2;
     for (int s = 0; s < n; ++s) {
         const Seg &sg = segs[s];
         GemmSeg &g = p.seg[s];
@@ -311,12 +334,12 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         if (wslot[sg.wkind] < 0) {
             if (nmaps >= GEMM_MAX_MAPS) return fail(c, RWKV7_ECUDA, "too many tensor maps in one GEMM");
             wslot[sg.wkind] = nmaps;
-            p.maps[nmaps++] = c->wmap[sg.wkind];
+            p.maps[nmaps++] = w8 ? (kbs8 == 2 ? c->wmap8[sg.wkind] : c->wmap8_1[sg.wkind]) : c->wmap[sg.wkind];
         }
         if (aslot[sg.xbuf] < 0) {
             if (nmaps >= GEMM_MAX_MAPS) return fail(c, RWKV7_ECUDA, "too many tensor maps in one GEMM");
             const int np16 = (B + 15) / 16 * 16;
-            const CUtensorMap *am3 = get_amap3(c, sg.xbuf, np16);
+            const CUtensorMap *am3 = (!w8 || kbs8 == 2) ? get_amap3(c, sg.xbuf, np16) : nullptr;
             const CUtensorMap *am = am3 ? am3 : get_amap(c, sg.xbuf, np16);
             if (!am) return RWKV7_ECUDA;
             aslot[sg.xbuf] = nmaps;
@@ -337,7 +360,9 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         g.ldo = sg.ldo;
         g.split_stride = (long long)c->bcap * sg.ldo;
         g.bias = sg.bias;
-        g.w = c->w[sg.wkind] + (size_t)(per_layer(sg.wkind) ? layer : 0) * layer_elems(c, sg.wkind);
+        g.w = w8 ? nullptr : c->w[sg.wkind] + (size_t)(per_layer(sg.wkind) ? layer : 0) * layer_elems(c, sg.wkind);
+        g.wscale = w8 ? c->wsc[sg.wkind] + (size_t)(per_layer(sg.wkind) ? layer : 0) * g.tiles * GEMM_TILE_M
+                      : nullptr;
         g.x = sg.xptr;
         g.ldx = sg.K;
         if (mode == 2) {
@@ -358,7 +383,24 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
     p.err = c->errw;
     cudaError_t e = cudaSuccess;
     if (mode == 2) {
+        if (w8) return fail(c, RWKV7_EINVAL, "the CUDA-core GEMM takes fp16 weights only");
         launch_gemm_simt(p, lc, &e);
+    } else if (w8) {
+        // ring A (int8 tiles + activations) as deep as fits beside two stages of
+        // converted fp16 tiles; one CTA per SM
+        const int SB = 2;
+        const size_t ab = (size_t)kbs8 * (GEMM_TILE_M * GEMM_TILE_K + (size_t)p.npad * 128);
+        const size_t bb = (size_t)kbs8 * GEMM_TILE_M * GEMM_TILE_K * 2;
+        const size_t budget = (size_t)gemm_tc_max_smem() - 2048 - SB * bb;
+        const int SA = (int)std::min<size_t>(8, budget / ab);
+        if (SA < 2) return fail(c, RWKV7_ECUDA, "internal: int8 GEMM ring does not fit");
+        p.stages = SA;
+        p.stages_b = SB;
+        p.kbs = kbs8;
+        p.accbufs = (2 * p.npad <= 512) ? 2 : 1;
+        p.prefetch = nz_skip == nullptr ? 1 : 0;
+        const int grid = std::min(p.nitems, c->nsm);
+        launch_gemm_tc8(p, grid, gemm_tc8_smem_bytes(p.npad, kbs8, SA, SB), lc, &e);
     } else {
         // CTAs per SM and pipeline depth: by default one CTA per SM with the
         // deepest pipeline that fits; RWKV7_GEMM_CTAS_PER_SM / RWKV7_GEMM_STAGES
@@ -369,6 +411,7 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         int stages = (int)std::min<size_t>(6, budget / stage);
         stages = std::max(2, std::min(stages, env_int("RWKV7_GEMM_STAGES", stages)));
         p.stages = stages;
+        p.kbs = 2;
         // Two accumulators (the next item's MMAs overlap this item's epilogue)
         // when they fit in the 512 TMEM columns; a CTA of this kernel always
         // has its SM to itself (its shared memory is over half of the SM's),
@@ -1029,8 +1072,13 @@ int parse_name(rwkv7_ctx *c, const char *name, int *kind, int *layer) {
 extern "C" {
 
 int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
+    return rwkv7_create_ex(cfg, 16, cuda_stream, out);
+}
+
+int rwkv7_create_ex(const rwkv7_config *cfg, int32_t weight_bits, void *cuda_stream, rwkv7_ctx **out) {
     if (!cfg || !out) return RWKV7_EINVAL;
     *out = nullptr;
+    if (weight_bits != 16 && weight_bits != 8) return RWKV7_EINVAL;
     const rwkv7_config &g = *cfg;
     if (g.head_size != HS || g.n_layer < 1 || g.d_model < HS || g.d_model % HS || g.d_model > 8192 ||
         g.d_ffn < 64 || g.d_ffn % 64 || g.vocab < 1 || g.n_slots < 1 || g.n_slots > 65536)
@@ -1040,6 +1088,7 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
     if (g.vocab % 8) return RWKV7_EINVAL;
     rwkv7_ctx *c = new rwkv7_ctx();
     c->cfg = g;
+    c->wbits = weight_bits;
     c->L = g.n_layer;
     c->d = g.d_model;
     c->H = g.d_model / HS;
@@ -1083,7 +1132,12 @@ int rwkv7_create(const rwkv7_config *cfg, void *cuda_stream, rwkv7_ctx **out) {
     for (int k : tc_kinds) c->tiled[k] = true;
     for (int k = 0; k < W_COUNT; ++k) {
         const size_t layers = per_layer(k) ? L : 1;
-        if ((rc = dalloc(c, &c->w[k], layers * layer_elems(c, k)))) return bad(rc);
+        if (c->wbits == 8 && c->tiled[k]) {
+            if ((rc = dalloc(c, &c->w8[k], layers * layer_elems(c, k)))) return bad(rc);
+            if ((rc = dalloc(c, &c->wsc[k], layers * (size_t)row_tiles(c, k) * GEMM_TILE_M))) return bad(rc);
+        } else if ((rc = dalloc(c, &c->w[k], layers * layer_elems(c, k)))) {
+            return bad(rc);
+        }
         c->n_missing += layers;
     }
     for (int k : tc_kinds)
@@ -1176,6 +1230,8 @@ int rwkv7_set_weight(rwkv7_ctx *c, const char *name, const void *host_f16, size_
     int kind, layer;
     if (parse_name(c, name, &kind, &layer)) return fail(c, RWKV7_ESHAPE, "unknown weight name '%s'", name);
     const size_t n = (size_t)c->wrows[kind] * c->wcols[kind];
+    if (c->wbits == 8 && c->tiled[kind])
+        return fail(c, RWKV7_ESHAPE, "'%s' is an int8 matrix in this context: use rwkv7_set_weight_i8", name);
     if (bytes != n * 2) return fail(c, RWKV7_ESHAPE, "'%s': %zu bytes given, %zu expected", name, bytes, n * 2);
     if (c->tiled[kind]) {
         // repack [rows][cols] into zero-padded 128 x 64 tiles, tile order (row tile, k-block)
@@ -1201,6 +1257,42 @@ int rwkv7_set_weight(rwkv7_ctx *c, const char *name, const void *host_f16, size_
     }
     return RWKV7_OK;
 }
+
+int rwkv7_set_weight_i8(rwkv7_ctx *c, const char *name, const int8_t *host_q, size_t q_bytes,
+                        const void *host_scale_f16, size_t scale_bytes) {
+    if (!c) return RWKV7_EINVAL;
+    if (!name || !host_q || !host_scale_f16) return fail(c, RWKV7_EINVAL, "null argument");
+    int kind, layer;
+    if (parse_name(c, name, &kind, &layer)) return fail(c, RWKV7_ESHAPE, "unknown weight name '%s'", name);
+    if (c->wbits != 8 || !c->tiled[kind])
+        return fail(c, RWKV7_ESHAPE, "'%s' is not an int8 matrix in this context", name);
+    const int rows = c->wrows[kind], cols = c->wcols[kind], kb = kblocks(c, kind), tiles = row_tiles(c, kind);
+    if (q_bytes != (size_t)rows * cols || scale_bytes != (size_t)rows * 2)
+        return fail(c, RWKV7_ESHAPE, "'%s': %zu + %zu bytes given, %zu + %zu expected", name, q_bytes, scale_bytes,
+                    (size_t)rows * cols, (size_t)rows * 2);
+    // repack [rows][cols] int8 into zero-padded 128 x 64 tiles, tile order (row tile, k-block)
+    std::vector<int8_t> t(layer_elems(c, kind), 0);
+    for (int r = 0; r < rows; ++r)
+        for (int k0 = 0; k0 < cols; k0 += GEMM_TILE_K) {
+            const int nk = std::min(GEMM_TILE_K, cols - k0);
+            int8_t *dst = t.data() + (((size_t)(r / GEMM_TILE_M) * kb + k0 / GEMM_TILE_K) * GEMM_TILE_M +
+                                      (r % GEMM_TILE_M)) * GEMM_TILE_K;
+            memcpy(dst, host_q + (size_t)r * cols + k0, (size_t)nk);
+        }
+    std::vector<__half> sc((size_t)tiles * GEMM_TILE_M, __float2half(0.0f));
+    memcpy(sc.data(), host_scale_f16, (size_t)rows * 2);
+    CK(cudaMemcpy(c->w8[kind] + (size_t)layer * t.size(), t.data(), t.size(), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(c->wsc[kind] + (size_t)layer * sc.size(), sc.data(), sc.size() * sizeof(__half),
+                  cudaMemcpyHostToDevice));
+    uint8_t &f = c->wset[(size_t)kind * c->L + layer];
+    if (!f) {
+        f = 1;
+        c->n_missing--;
+    }
+    return RWKV7_OK;
+}
+
+int32_t rwkv7_weight_bits(const rwkv7_ctx *c) { return c ? c->wbits : 0; }
 
 int rwkv7_load_weights(rwkv7_ctx *c, const char *path) {
     if (!c) return RWKV7_EINVAL;
@@ -1470,6 +1562,8 @@ int rwkv7_synchronize(rwkv7_ctx *c) {
 int rwkv7_set_mode(rwkv7_ctx *c, int32_t mode) {
     if (!c) return RWKV7_EINVAL;
     if (mode < 0 || mode > 3) return fail(c, RWKV7_EINVAL, "mode must be 0, 1, 2 or 3");
+    if (c->wbits == 8 && mode >= 2)
+        return fail(c, RWKV7_EINVAL, "int8 weights run in modes 0 and 1 (tensor-core kernels) only");
     c->mode = mode;
     return RWKV7_OK;
 }
