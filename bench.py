@@ -87,6 +87,17 @@ def step_bytes(dm: synth.Dims, B: int) -> int:
     return w + s
 
 
+def step_bytes_i8(dm: synth.Dims, B: int) -> int:
+    """step_bytes for the int8 weight variant: one byte per matrix weight plus
+    an fp16 scale per matrix row, the same states."""
+    d, F, V, L, H = dm.d_model, dm.d_ffn, dm.vocab, dm.n_layer, dm.n_head
+    rs = dm.lora_w + dm.lora_a + dm.lora_v + dm.lora_g
+    w = L * (4 * d * d + 2 * d * F + 2 * d * rs) + V * d
+    scales = (L * (4 * d + F + d + rs + 4 * d) + V) * 2  # rows of r,k,v,o, key, value, LoRA down and up, head
+    s = 2 * B * L * (H * 64 * 64 + 2 * d) * 4
+    return w + scales + s
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed region runs."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -281,18 +292,25 @@ def run_trace_bench(args, wl):
     return 0
 
 
-def secondary(config, steps, args, dev, world):
+def secondary(config, steps, args, dev, world, int8=False):
     """The same timed decode loop on another named workload (graph replay,
-    CUDA events, clocks sampled): throughput and whole-step roofline."""
+    CUDA events, clocks sampled): throughput and whole-step roofline.  int8:
+    the int8 weight variant (synth.make_weights_i8) of the workload."""
     import torch
     import recurrent_decode_gb300 as rd
     wl = synth.WORKLOADS[config]
     dm = synth.Dims(wl["shape"])
     B = wl["B"]
-    weights = synth.make_weights(wl["shape"])
-    ctx = rd.Rwkv7(dm, B)
-    ctx.set_weights(weights)
-    del weights
+    if int8:
+        w16, i8 = synth.make_weights_i8(wl["shape"])
+        ctx = rd.Rwkv7(dm, B, weight_bits=8)
+        ctx.set_weights(w16, i8)
+        del w16, i8
+    else:
+        weights = synth.make_weights(wl["shape"])
+        ctx = rd.Rwkv7(dm, B)
+        ctx.set_weights(weights)
+        del weights
     if args.mode >= 0:
         ctx.set_mode(args.mode)
     for s in range(B):
@@ -333,9 +351,13 @@ def secondary(config, steps, args, dev, world):
     ctx.synchronize()
     ctx.close()
     peak, peak_kind = _peaks()
-    sb = step_bytes(dm, B)
+    sb = step_bytes_i8(dm, B) if int8 else step_bytes(dm, B)
     gbs = sb / (ms / steps / 1e3) / 1e9
-    return {"config": _config(wl, dm, argparse.Namespace(steps=steps)), "value": world * B * steps / (ms / 1e3),
+    cfg = _config(wl, dm, argparse.Namespace(steps=steps))
+    if int8:
+        cfg["workload"] += ", int8 weights"
+        cfg["weights"] = "random-init int8 matrices (uniform on [-127, 127]) with fp16 row scales (seed 0)"
+    return {"config": cfg, "value": world * B * steps / (ms / 1e3),
             "unit": "tok/s", "steps": steps, "ms_per_step": ms / steps,
             "step_roofline": {"bytes_per_step": sb, "achieved_GBps": gbs, "frac_of_peak": gbs / peak,
                               "peak_kind": peak_kind, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS},
@@ -518,6 +540,8 @@ def main():
     if args.config == "2.9b" and world == 1 and not args.layers and not args.prompt and not args.no_secondary:
         # the metric names both shapes: the 7.2B workload rides along on the same line
         line["secondary"] = secondary("7.2b", max(16, min(64, args.steps)), args, dev, world)
+        # the int8 weight variant of the headline workload (a separate row, not the headline)
+        line["int8"] = secondary("2.9b", max(16, min(256, args.steps)), args, dev, world, int8=True)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

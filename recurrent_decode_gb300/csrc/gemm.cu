@@ -442,28 +442,35 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
 
 // ---------------------------------------------------------------------------
 // int8-weight variant.  A weight tile arrives as 128 rows x 64 int8 (8 KB; the
-// int8 tiles keep the fp16 tile order) and is widened to fp16 in shared memory
-// before tcgen05.mma kind::f16 reads it; the row scale multiplies the finished
-// sum in the epilogue (W = q * scale per row, so W x = scale * (q x)).
-// Two rings: ring A holds, per stage, the int8 tiles of kbs k-blocks and the
-// activation boxes; ring B the converted fp16 tiles in the SW128 K-major layout
-// the TMA would have produced (16-byte chunk c of row r at chunk c ^ (r & 7)).
+// int8 tiles keep the fp16 tile order), is widened to fp16 in registers and
+// stored into tensor memory, from where tcgen05.mma kind::f16 reads it as the
+// A operand; the row scale multiplies the finished sum in the epilogue (W = q *
+// scale per row, so W x = scale * (q x)).
+// Shared memory holds one ring (A) of stages: the int8 tiles of kbs k-blocks
+// (TMA, 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3), so
+// that a warp reading one chunk of 32 rows hits every bank once) and the
+// activation boxes.  Tensor memory holds the accumulators and SB stages of
+// widened weights (kbs x 32 columns each).
 // Roles: warp 0 lane 0 loads ring A (the int8 tiles of the first stages before
 // the dependency wait); warp 1 lane 0 issues the MMAs; the 16 epilogue warps
-// convert ring A's int8 tiles into ring B while the mainloop runs and run the
-// epilogue after each item.  Barriers: full_w / full_x (int8 / activation bytes
-// of a ring A stage landed), empty_a (16 converter warps + the MMA commit),
-// full_b (16 converter warps), empty_b (the MMA commit).
+// form four groups of four (one warp per TMEM lane quarter = 32 weight rows,
+// one row per lane) that widen stages q with q % 4 == group, so four stages
+// are in flight, and run the epilogue after each item.  The host takes
+// exactly four weight stages (SB) and a ring A depth (SA) that is a multiple
+// of four: a slot's previous stage then belongs to the same group, which has
+// already waited on it, so no barrier is waited on two phases ahead.  Barriers: full_w /
+// full_x (int8 / activation bytes of a ring A stage landed), empty_a (the
+// group's 4 warps + the MMA commit), full_b (the group's 4 warps), empty_b
+// (the MMA commit).
 // ---------------------------------------------------------------------------
 constexpr uint32_t W8_TILE_BYTES = GEMM_TILE_M * GEMM_TILE_K;  // 8 KB
+constexpr int CONV_GROUPS = EPI_WARPS / 4;
 
-// 16 int8 (one 16-byte chunk) -> 16 fp16 at two swizzled 16-byte chunks.  Exact:
-// the byte x ^ 0x80 = x + 128 is placed in the low mantissa byte of the fp16
-// 1024.0 (0x6400), giving 1024 + 128 + x, and 1152 is subtracted.
-__device__ __forceinline__ void widen16(const uint8_t *src, uint8_t *dst_row, int g, int r) {
-    const uint4 in = *reinterpret_cast<const uint4 *>(src);
+// 16 int8 -> 8 words of two fp16 each (element 2j in the low half of word j).
+// Exact: the byte x ^ 0x80 = x + 128 is placed in the low mantissa byte of the
+// fp16 1024.0 (0x6400), giving 1024 + 128 + x, and 1152 is subtracted.
+__device__ __forceinline__ void widen16(const uint4 in, uint32_t *o) {
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    uint32_t o[8];
     const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6480u),
                                        __ushort_as_half((unsigned short)0x6480u));  // 1152
 #pragma unroll
@@ -476,9 +483,6 @@ __device__ __forceinline__ void widen16(const uint8_t *src, uint8_t *dst_row, in
         o[2 * k] = *reinterpret_cast<uint32_t *>(&hl);
         o[2 * k + 1] = *reinterpret_cast<uint32_t *>(&hh);
     }
-    const int c0 = 2 * g, c1 = 2 * g + 1, sw = r & 7;
-    *reinterpret_cast<uint4 *>(dst_row + ((c0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4 *>(dst_row + ((c1 ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 __device__ __forceinline__ bool stage_skipped_k(const uint32_t *flags, int kb, int kbs) {
@@ -500,10 +504,8 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
     const uint32_t W8B = (uint32_t)KBS * W8_TILE_BYTES;  // int8 tiles of a stage
     const uint32_t XB = (uint32_t)KBS * XKB;            // activations of a stage
     const uint32_t AB = W8B + XB;                       // ring A stage (a multiple of 1024)
-    const uint32_t W16B = (uint32_t)KBS * W_TILE_BYTES; // ring B stage
     uint8_t *sA = base;
-    uint8_t *sB = base + (size_t)SA * AB;
-    uint64_t *full_w = (uint64_t *)(sB + (size_t)SB * W16B);
+    uint64_t *full_w = (uint64_t *)(sA + (size_t)SA * AB);
     uint64_t *full_x = full_w + SA;
     uint64_t *empty_a = full_x + SA;
     uint64_t *full_b = empty_a + SA;
@@ -517,18 +519,18 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int i_begin = item_first(c, G, nitems), i_end = item_first(c + 1, G, nitems);
-    uint32_t ncols = 32;
-    while ((int)ncols < NB * npad) ncols <<= 1;
+    const uint32_t ncols = 512;                        // accumulators + widened weight stages
+    const uint32_t acol0 = (uint32_t)(NB * npad);      // first column of the weight stages
 
     if (threadIdx.x < nseg) sseg[threadIdx.x] = p.seg[threadIdx.x];
     if (threadIdx.x == 0) {
         for (int i = 0; i < SA; ++i) {
             mbar_init(&full_w[i], 1);
             mbar_init(&full_x[i], 1);
-            mbar_init(&empty_a[i], EPI_WARPS + 1);
+            mbar_init(&empty_a[i], 4 + 1);
         }
         for (int i = 0; i < SB; ++i) {
-            mbar_init(&full_b[i], EPI_WARPS);
+            mbar_init(&full_b[i], 4);
             mbar_init(&empty_b[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -643,14 +645,13 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sB + (size_t)sb * W16B);
+                    const uint32_t a0 = tmem + acol0 + (uint32_t)(sb * KBS * 32);
                     const uint32_t b0 = smem_u32(sA + (size_t)sa * AB + W8B);
                     for (int h = 0; h < KBS; ++h) {
 #pragma unroll
                         for (int kk = 0; kk < GEMM_TILE_K / 16; ++kk)
-                            mma_f16(d_tmem, sdesc_k128(a0 + h * W_TILE_BYTES + kk * 32),
-                                    sdesc_k128(b0 + h * XKB + kk * 32), idesc,
-                                    (issued | (uint32_t)h | (uint32_t)kk) ? 1u : 0u);
+                            mma_f16_ts(d_tmem, a0 + (uint32_t)(h * 32 + kk * 8), sdesc_k128(b0 + h * XKB + kk * 32),
+                                       idesc, (issued | (uint32_t)h | (uint32_t)kk) ? 1u : 0u);
                     }
                     issued = 1;
                     mma_commit(&empty_a[sa]);
@@ -670,10 +671,11 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
         }
     } else {
         // ------------------------------------------------ converters + epilogue
-        const int qd = warp & 3;
+        const int qd = warp & 3;              // TMEM lane quarter = weight rows qd*32 .. +31
         const int row = qd * 32 + lane;
         const int et = threadIdx.x - 64;
-        const int grp = et >> 7;
+        const int grp = et >> 7;              // converter group: stages q with q % 4 == grp
+        const uint32_t tlane = (uint32_t)(qd * 32) << 16;
         uint32_t *nz_out = p.nz_out;
         bool waited = false;
         if (has_skip) {
@@ -692,18 +694,16 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
             const GemmSeg sg = sseg[it.s];
             const int buf = n % NB;
             bool valid = false;
-            // convert this item's stages (each thread: KBS 16-byte int8 chunks per stage)
             for (int kb = it.kb0; kb < it.kb1; kb += KBS) {
                 if (stage_skipped_k(skip, kb, KBS)) continue;
                 valid = true;
-                const int sa = q % SA, sb = q % SB;
-                ++q;
-                if (dead) continue;  // an earlier wait gave up: convert nothing more
+                const int qq = q++;
+                if (qq % CONV_GROUPS != grp || dead) continue;  // another group's stage
+                const int sa = qq % SA, sb = qq % SB;
                 uint32_t w_ok = 0u;
                 if (lane == 0) {
-                    bool okw = mbar_wait(&full_w[sa], (uint32_t)((q - 1) / SA) & 1u, abort_flag);
-                    if (okw && q - 1 >= SB)
-                        okw = mbar_wait(&empty_b[sb], (uint32_t)(((q - 1) / SB) - 1) & 1u, abort_flag);
+                    bool okw = mbar_wait(&full_w[sa], (uint32_t)(qq / SA) & 1u, abort_flag);
+                    if (okw && qq >= SB) okw = mbar_wait(&empty_b[sb], (uint32_t)((qq / SB) - 1) & 1u, abort_flag);
                     if (!okw) {
                         *abort_flag = 1u;
                         atomicOr(p.err, ERR_TIMEOUT);
@@ -715,17 +715,24 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
                     dead = true;
                     continue;
                 }
-                // acquire the landed int8 bytes / the released fp16 stage in every lane
-                (void)mbar_try_wait(&full_w[sa], (uint32_t)((q - 1) / SA) & 1u);
-                if (q - 1 >= SB) (void)mbar_try_wait(&empty_b[sb], (uint32_t)(((q - 1) / SB) - 1) & 1u);
-                const uint8_t *a8 = sA + (size_t)sa * AB;
-                uint8_t *b16 = sB + (size_t)sb * W16B;
-                for (int u = et; u < KBS * 512; u += EPI_THREADS) {
-                    const int h = u >> 9, r = (u >> 2) & 127, g = u & 3;
-                    widen16(a8 + (size_t)h * W8_TILE_BYTES + r * 64 + g * 16,
-                            b16 + (size_t)h * W_TILE_BYTES + r * 128, g, r);
+                // acquire the landed int8 bytes / the released weight stage in every lane
+                (void)mbar_try_wait(&full_w[sa], (uint32_t)(qq / SA) & 1u);
+                if (qq >= SB) (void)mbar_try_wait(&empty_b[sb], (uint32_t)((qq / SB) - 1) & 1u);
+                tc_fence_after();
+                const uint8_t *a8 = sA + (size_t)sa * AB + row * 64;
+                const int sw = (row >> 1) & 3;
+                for (int h = 0; h < KBS; ++h) {
+                    uint32_t o[32];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint4 in =
+                            *reinterpret_cast<const uint4 *>(a8 + (size_t)h * W8_TILE_BYTES + ((cc ^ sw) << 4));
+                        widen16(in, o + 8 * cc);
+                    }
+                    tmem_st32(tmem + tlane + acol0 + (uint32_t)(sb * KBS * 32 + h * 32), o);
                 }
-                fence_proxy_async();  // generic-proxy writes -> visible to the tensor cores
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&full_b[sb]);
@@ -750,7 +757,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
             }
             (void)mbar_try_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u);
             tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
+            const uint32_t taddr = tmem + tlane + (uint32_t)(buf * npad);
             const int nrow = it.tile * GEMM_TILE_M + row;
             const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B, grp * EPI_CW);
             tc_fence_before();
@@ -788,10 +795,9 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
     }
 }
 
-size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a, int stages_b) {
+size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a) {
     const size_t ab = (size_t)kbs * (W8_TILE_BYTES + (size_t)npad * 128);
-    const size_t bb = (size_t)kbs * W_TILE_BYTES;
-    return 1024 + (size_t)stages_a * ab + (size_t)stages_b * bb + (size_t)(3 * stages_a + 2 * stages_b + 4) * 8 + 64;
+    return 1024 + (size_t)stages_a * ab + (size_t)(3 * stages_a + 2 * 8 + 4) * 8 + 64;
 }
 
 void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e) {

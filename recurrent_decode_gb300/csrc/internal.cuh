@@ -72,7 +72,7 @@ struct GemmParams {
     int nseg, nmaps, nitems;
     int B, npad;                     // slots in the step, MMA N (B rounded up to 16)
     int stages;                      // smem pipeline depth (int8 weights: stages of the int8 + activation ring)
-    int stages_b;                    // int8 weights: stages of the converted fp16 weight ring
+    int stages_b;                    // int8 weights: stages of widened weights in tensor memory
     int kbs;                         // int8 weights: k-blocks per stage (1 or 2); fp16 weights: always 2
     int accbufs;                     // TMEM accumulator buffers (1 or 2)
     int prefetch;                    // 1: weights may be fetched before the dependency wait
@@ -94,7 +94,7 @@ size_t gemm_tc_smem_bytes(int npad, int stages);
 // int8-weight GEMM: weights arrive as int8 tiles and are converted to fp16 in
 // shared memory by the epilogue warps before the tensor cores read them.
 void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e);
-size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a, int stages_b);
+size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a);
 size_t gemm_tc_stage_bytes(int npad);
 int gemm_tc_max_smem();
 
@@ -421,6 +421,31 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         : "memory");
 }
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread completes.
+// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulate: A (M = 128
+// rows) read from tensor memory, row m in lane m, fp16 elements (2j, 2j + 1)
+// of its K slice packed in column j (low half first).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 32 lanes x 32 columns of 32-bit values from registers into tensor memory
+// (lane i of the warp -> TMEM lane base + i, register j -> column base + j).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))

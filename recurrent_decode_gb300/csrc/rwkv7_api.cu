@@ -197,10 +197,11 @@ int make_map(rwkv7_ctx *c, CUtensorMap *m, void *base, int rank, const uint64_t 
     }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
     // fp16 tiles land in the SW128 K-major layout the tensor cores read; int8
-    // tiles land row-major (64 bytes a row) and are widened by the kernel
+    // tiles (64-byte rows) land with the 64-byte swizzle and are widened by the
+    // kernel
     CUresult r = fn(m, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank,
                     base, gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    int8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(c, RWKV7_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return RWKV7_OK;
@@ -386,21 +387,25 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         if (w8) return fail(c, RWKV7_EINVAL, "the CUDA-core GEMM takes fp16 weights only");
         launch_gemm_simt(p, lc, &e);
     } else if (w8) {
-        // ring A (int8 tiles + activations) as deep as fits beside two stages of
-        // converted fp16 tiles; one CTA per SM
-        const int SB = 2;
+        // Tensor memory: the accumulators and four stages of widened weights
+        // (kbs8 x 32 columns each) in its 512 columns.  Stage q is widened by
+        // converter group q % 4, so with four weight stages each stage slot has
+        // one group, and with a ring A depth that is a multiple of four each
+        // ring A slot's previous stage was waited on by the same group: no
+        // barrier is ever waited on two phases ahead.  One CTA per SM.
+        p.kbs = kbs8;
+        const int SB = 4;
+        p.accbufs = (2 * p.npad + SB * kbs8 * 32 <= 512) ? 2 : 1;
         const size_t ab = (size_t)kbs8 * (GEMM_TILE_M * GEMM_TILE_K + (size_t)p.npad * 128);
-        const size_t bb = (size_t)kbs8 * GEMM_TILE_M * GEMM_TILE_K * 2;
-        const size_t budget = (size_t)gemm_tc_max_smem() - 2048 - SB * bb;
-        const int SA = (int)std::min<size_t>(8, budget / ab);
-        if (SA < 2) return fail(c, RWKV7_ECUDA, "internal: int8 GEMM ring does not fit");
+        const size_t budget = (size_t)gemm_tc_max_smem() - 2048;
+        const int SA = budget / ab >= 8 ? 8 : 4;
+        if (budget / ab < 4 || p.accbufs * p.npad + SB * kbs8 * 32 > 512)
+            return fail(c, RWKV7_ECUDA, "internal: int8 GEMM buffers do not fit");
         p.stages = SA;
         p.stages_b = SB;
-        p.kbs = kbs8;
-        p.accbufs = (2 * p.npad <= 512) ? 2 : 1;
         p.prefetch = nz_skip == nullptr ? 1 : 0;
         const int grid = std::min(p.nitems, c->nsm);
-        launch_gemm_tc8(p, grid, gemm_tc8_smem_bytes(p.npad, kbs8, SA, SB), lc, &e);
+        launch_gemm_tc8(p, grid, gemm_tc8_smem_bytes(p.npad, kbs8, SA), lc, &e);
     } else {
         // CTAs per SM and pipeline depth: by default one CTA per SM with the
         // deepest pipeline that fits; RWKV7_GEMM_CTAS_PER_SM / RWKV7_GEMM_STAGES
