@@ -33,10 +33,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram bytes per launch from ncu captures, valid only while the kernel source is
 # unchanged: kernel -> (source file, sha256 prefix of it at capture, workload, bytes)
 NCU_TRAFFIC = {
-    ("gemm_tc_kernel", "2.9b"): ("recurrent_decode_gb300/csrc/gemm.cu", "949b7b5652f87b5a",
+    ("gemm_tc_kernel", "2.9b"): ("recurrent_decode_gb300/csrc/gemm.cu", "3fb1af53aa13b82e",
                                   "2.9B shape, B=64: DRAM read+write of the 11 GEMM launches of one step of "
                                   "a 2-layer cut (profiles/gemm_traffic_2.9b_b64.md), scaled to 32 layers + head, "
-                                  "per launch", 35822085),
+                                  "per launch", 35823667),
 }
 
 

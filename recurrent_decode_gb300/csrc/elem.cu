@@ -479,7 +479,6 @@ __global__ void __launch_bounds__(64) wkv_vec_kernel(const WkvSeqParams p) {
 // per token as 6 x 64 contiguous floats, so 32 tokens are one 48 KB block: one
 // bulk copy per block, two blocks in flight.
 constexpr int WSQ_TB = 32;
-constexpr uint32_t WSQ_BLOCK = WSQ_TB * 6 * HS * 4;  // bytes
 struct WsqSmem {
     float vec[2][WSQ_TB][6][HS];
     uint64_t full[2];
