@@ -446,25 +446,29 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
 // stored into tensor memory, from where tcgen05.mma kind::f16 reads it as the
 // A operand; the row scale multiplies the finished sum in the epilogue (W = q *
 // scale per row, so W x = scale * (q x)).
-// Shared memory holds one ring (A) of stages: the int8 tiles of kbs k-blocks
-// (TMA, 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3), so
-// that a warp reading one chunk of 32 rows hits every bank once) and the
-// activation boxes.  Tensor memory holds the accumulators and SB stages of
-// widened weights (kbs x 32 columns each).
-// Roles: warp 0 lane 0 loads ring A (the int8 tiles of the first stages before
-// the dependency wait); warp 1 lane 0 issues the MMAs; the 16 epilogue warps
-// form four groups of four (one warp per TMEM lane quarter = 32 weight rows,
-// one row per lane) that widen stages q with q % 4 == group, so four stages
-// are in flight, and run the epilogue after each item.  The host takes
-// exactly four weight stages (SB) and a ring A depth (SA) that is a multiple
-// of four: a slot's previous stage then belongs to the same group, which has
-// already waited on it, so no barrier is waited on two phases ahead.  Barriers: full_w /
-// full_x (int8 / activation bytes of a ring A stage landed), empty_a (the
-// group's 4 warps + the MMA commit), full_b (the group's 4 warps), empty_b
-// (the MMA commit).
+// Shared memory: ring W (SA stages of the int8 tiles of kbs k-blocks, TMA with
+// the 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3), so that
+// a warp reading one chunk of 32 rows hits every bank once) and ring X (SX
+// stages of activation boxes).  Tensor memory: the accumulators and SB = 4
+// stages of widened weights (kbs x 32 columns each).
+// Roles: warp 0 lane 0 streams ring W from the first instant (weights are
+// constant: no dependency wait); warp 18 lane 0 loads ring X after the
+// dependency wait; warp 1 lane 0 issues the MMAs; the 16 epilogue warps form
+// four groups of four (one warp per TMEM lane quarter = 32 weight rows, one
+// row per lane) that widen stages q with q % 4 == group -- four stages in
+// flight -- and run the epilogue after each item.  A ring W slot is released
+// as soon as its group has widened it, so the int8 stream runs up to SA stages
+// ahead of the tensor cores.  SB = 4 and SA a multiple of 4 (chosen by the
+// host): a slot's previous stage then belongs to the same group, which has
+// already waited on it, so no barrier is ever waited on two phases ahead.
+// Barriers: full_w / empty_w (int8 bytes landed / the group's 4 warps),
+// full_x / empty_x (activation bytes landed / the MMA commit), full_b (the
+// group's 4 warps) / empty_b (the MMA commit).
 // ---------------------------------------------------------------------------
 constexpr uint32_t W8_TILE_BYTES = GEMM_TILE_M * GEMM_TILE_K;  // 8 KB
 constexpr int CONV_GROUPS = EPI_WARPS / 4;
+constexpr int GEMM_TC8_THREADS = GEMM_TC_THREADS + 32;          // + the activation producer warp
+constexpr int XPROD_WARP = GEMM_TC_THREADS / 32;
 
 // 16 int8 -> 8 words of two fp16 each (element 2j in the low half of word j).
 // Exact: the byte x ^ 0x80 = x + 128 is placed in the low mantissa byte of the
@@ -489,26 +493,27 @@ __device__ __forceinline__ bool stage_skipped_k(const uint32_t *flags, int kb, i
     return flags != nullptr && flags[kb] == 0u && (kbs == 1 || flags[kb + 1] == 0u);
 }
 
-__global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(GEMM_TC8_THREADS, 1) gemm_tc8_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ GemmSeg sseg[GEMM_MAX_SEG];
     __shared__ uint32_t snz[MAX_NZ_BLOCKS];
     __shared__ uint64_t flags_ready;
     __shared__ uint32_t s_ok;
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int SA = p.stages, SB = p.stages_b, KBS = p.kbs;
+    const int SA = p.stages, SB = p.stages_b, SX = p.stages_x, KBS = p.kbs;
     const int B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, nitems = p.nitems;
     const bool has_skip = p.nz_skip != nullptr;
     const uint32_t *skip = has_skip ? snz : nullptr;
     const uint32_t XKB = (uint32_t)npad * 128u;        // one activation k-block
-    const uint32_t W8B = (uint32_t)KBS * W8_TILE_BYTES;  // int8 tiles of a stage
-    const uint32_t XB = (uint32_t)KBS * XKB;            // activations of a stage
-    const uint32_t AB = W8B + XB;                       // ring A stage (a multiple of 1024)
-    uint8_t *sA = base;
-    uint64_t *full_w = (uint64_t *)(sA + (size_t)SA * AB);
-    uint64_t *full_x = full_w + SA;
-    uint64_t *empty_a = full_x + SA;
-    uint64_t *full_b = empty_a + SA;
+    const uint32_t W8B = (uint32_t)KBS * W8_TILE_BYTES;  // ring W stage (a multiple of 1024)
+    const uint32_t XB = (uint32_t)KBS * XKB;            // ring X stage (a multiple of 1024)
+    uint8_t *sW = base;
+    uint8_t *sX = base + (size_t)SA * W8B;
+    uint64_t *full_w = (uint64_t *)(sX + (size_t)SX * XB);
+    uint64_t *empty_w = full_w + SA;
+    uint64_t *full_x = empty_w + SA;
+    uint64_t *empty_x = full_x + SX;
+    uint64_t *full_b = empty_x + SX;
     uint64_t *empty_b = full_b + SB;
     uint64_t *acc_full = empty_b + SB;   // [2]
     uint64_t *acc_empty = acc_full + 2;  // [2]
@@ -526,8 +531,11 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
     if (threadIdx.x == 0) {
         for (int i = 0; i < SA; ++i) {
             mbar_init(&full_w[i], 1);
+            mbar_init(&empty_w[i], 4);
+        }
+        for (int i = 0; i < SX; ++i) {
             mbar_init(&full_x[i], 1);
-            mbar_init(&empty_a[i], 4 + 1);
+            mbar_init(&empty_x[i], 1);
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(&full_b[i], 4);
@@ -542,25 +550,8 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
         nzf[0] = nzf[1] = 0u;
         fence_barrier_init();
     }
-    __syncthreads();
-
-    // int8 tiles of the first stages before the dependency wait (weights are constant)
-    int npre = 0;
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0)
         for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.maps[i]);
-        if (p.prefetch) {
-            const uint64_t polW = policy_evict_first();
-            for (int i = i_begin; i < i_end && npre < SA; ++i) {
-                const Item it = locate_item(sseg, nseg, i);
-                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
-                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
-                for (int kb = it.kb0; kb < it.kb1 && npre < SA; kb += KBS, ++npre) {
-                    mbar_expect_tx(&full_w[npre], W8B);
-                    tma_load_3d(sA + (size_t)npre * AB, wm, &full_w[npre], 0, 0, tb + kb, polW);
-                }
-            }
-        }
-    }
     if (warp == 1) {
         tmem_alloc(tmem_slot, ncols);
         tmem_relinquish();
@@ -571,9 +562,41 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (ring A)
+        // ------------------------------------------------ int8 weight producer (ring W)
         if (lane == 0) {
-            const uint64_t polW = policy_evict_first(), polX = policy_evict_last();
+            const uint64_t polW = policy_evict_first();
+            bool ok = true;
+            // the skipped stages depend on flags the preceding kernel writes
+            if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
+            int q = 0;
+            for (int i = i_begin; i < i_end && ok; ++i) {
+                const Item it = locate_item(sseg, nseg, i);
+                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
+                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
+                for (int kb = it.kb0; kb < it.kb1; kb += KBS) {
+                    if (stage_skipped_k(skip, kb, KBS)) continue;
+                    const int st = q % SA;
+                    if (q >= SA && !mbar_wait(&empty_w[st], (uint32_t)((q / SA) - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&full_w[st], W8B);
+                    tma_load_3d(sW + (size_t)st * W8B, wm, &full_w[st], 0, 0, tb + kb, polW);
+                    ++q;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1u;
+                atomicOr(p.err, ERR_TIMEOUT);
+            }
+            // before leaving, wait (bounded) until no copy issued here is in flight
+            for (int j = (q > SA ? q - SA : 0); j < q; ++j)
+                if (!mbar_wait_any(&full_w[j % SA], (uint32_t)(j / SA) & 1u)) break;
+        }
+    } else if (warp == XPROD_WARP) {
+        // ------------------------------------------------ activation producer (ring X)
+        if (lane == 0) {
+            const uint64_t polX = policy_evict_last();
             pdl_wait();
             pdl_launch();
             bool ok = true;
@@ -581,27 +604,21 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
             int q = 0;
             for (int i = i_begin; i < i_end && ok; ++i) {
                 const Item it = locate_item(sseg, nseg, i);
-                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
-                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
                 const CUtensorMap *xm = &p.maps[sseg[it.s].xmap];
                 for (int kb = it.kb0; kb < it.kb1; kb += KBS) {
                     if (stage_skipped_k(skip, kb, KBS)) continue;
-                    const int st = q % SA;
-                    uint8_t *sa = sA + (size_t)st * AB;
-                    if (q >= npre) {
-                        if (q >= SA && !mbar_wait(&empty_a[st], (uint32_t)((q / SA) - 1) & 1u, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_expect_tx(&full_w[st], W8B);
-                        tma_load_3d(sa, wm, &full_w[st], 0, 0, tb + kb, polW);
+                    const int st = q % SX;
+                    if (q >= SX && !mbar_wait(&empty_x[st], (uint32_t)((q / SX) - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    uint8_t *sx = sX + (size_t)st * XB;
                     mbar_expect_tx(&full_x[st], XB);
                     if (sseg[it.s].x3) {
-                        tma_load_3d(sa + W8B, xm, &full_x[st], 0, 0, kb, polX);
+                        tma_load_3d(sx, xm, &full_x[st], 0, 0, kb, polX);
                     } else {
                         for (int h = 0; h < KBS; ++h)
-                            tma_load_2d(sa + W8B + (size_t)h * XKB, xm, &full_x[st], (kb + h) * GEMM_TILE_K, 0, polX);
+                            tma_load_2d(sx + (size_t)h * XKB, xm, &full_x[st], (kb + h) * GEMM_TILE_K, 0, polX);
                     }
                     ++q;
                 }
@@ -610,14 +627,8 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
                 *abort_flag = 1u;
                 atomicOr(p.err, ERR_TIMEOUT);
             }
-            // Before leaving, wait (bounded) until no copy issued here is in flight:
-            // int8 tiles of stages < max(q, npre) (prefetched ones may be ahead of
-            // q after an abort), activations of stages < q.
-            const int qw = q > npre ? q : npre;
-            for (int j = (qw > SA ? qw - SA : 0); j < qw; ++j)
-                if (!mbar_wait_any(&full_w[j % SA], (uint32_t)(j / SA) & 1u)) break;
-            for (int j = (q > SA ? q - SA : 0); j < q; ++j)
-                if (!mbar_wait_any(&full_x[j % SA], (uint32_t)(j / SA) & 1u)) break;
+            for (int j = (q > SX ? q - SX : 0); j < q; ++j)
+                if (!mbar_wait_any(&full_x[j % SX], (uint32_t)(j / SX) & 1u)) break;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -638,15 +649,15 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
                 uint32_t issued = 0;
                 for (int kb = it.kb0; kb < it.kb1; kb += KBS) {
                     if (stage_skipped_k(skip, kb, KBS)) continue;
-                    const int sa = q % SA, sb = q % SB;
-                    if (!mbar_wait(&full_x[sa], (uint32_t)(q / SA) & 1u, abort_flag) ||
+                    const int sx = q % SX, sb = q % SB;
+                    if (!mbar_wait(&full_x[sx], (uint32_t)(q / SX) & 1u, abort_flag) ||
                         !mbar_wait(&full_b[sb], (uint32_t)(q / SB) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a0 = tmem + acol0 + (uint32_t)(sb * KBS * 32);
-                    const uint32_t b0 = smem_u32(sA + (size_t)sa * AB + W8B);
+                    const uint32_t b0 = smem_u32(sX + (size_t)sx * XB);
                     for (int h = 0; h < KBS; ++h) {
 #pragma unroll
                         for (int kk = 0; kk < GEMM_TILE_K / 16; ++kk)
@@ -654,7 +665,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
                                        idesc, (issued | (uint32_t)h | (uint32_t)kk) ? 1u : 0u);
                     }
                     issued = 1;
-                    mma_commit(&empty_a[sa]);
+                    mma_commit(&empty_x[sx]);
                     mma_commit(&empty_b[sb]);
                     ++q;
                 }
@@ -719,7 +730,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
                 (void)mbar_try_wait(&full_w[sa], (uint32_t)(qq / SA) & 1u);
                 if (qq >= SB) (void)mbar_try_wait(&empty_b[sb], (uint32_t)((qq / SB) - 1) & 1u);
                 tc_fence_after();
-                const uint8_t *a8 = sA + (size_t)sa * AB + row * 64;
+                const uint8_t *a8 = sW + (size_t)sa * W8B + row * 64;
                 const int sw = (row >> 1) & 3;
                 for (int h = 0; h < KBS; ++h) {
                     uint32_t o[32];
@@ -731,13 +742,12 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
                     }
                     tmem_st32(tmem + tlane + acol0 + (uint32_t)(sb * KBS * 32 + h * 32), o);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_w[sa]);  // the int8 bytes are read: the slot may refill
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&full_b[sb]);
-                    mbar_arrive(&empty_a[sa]);
-                }
+                if (lane == 0) mbar_arrive(&full_b[sb]);
             }
             if (!waited) {  // outputs may be read by the preceding kernel until it completes
                 pdl_wait();
@@ -795,9 +805,9 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc8_kernel(const __gr
     }
 }
 
-size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a) {
-    const size_t ab = (size_t)kbs * (W8_TILE_BYTES + (size_t)npad * 128);
-    return 1024 + (size_t)stages_a * ab + (size_t)(3 * stages_a + 2 * 8 + 4) * 8 + 64;
+size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_w, int stages_x) {
+    return 1024 + (size_t)stages_w * kbs * W8_TILE_BYTES + (size_t)stages_x * kbs * npad * 128 +
+           (size_t)(2 * stages_w + 2 * stages_x + 2 * 8 + 4) * 8 + 64;
 }
 
 void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e) {
@@ -813,7 +823,7 @@ void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(GEMM_TC_THREADS);
+    cfg.blockDim = dim3(GEMM_TC8_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = lc.stream;
     cudaLaunchAttribute at[1];
@@ -821,7 +831,7 @@ void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = lc.pdl ? 1 : 0;
-    cudaError_t r = cudaLaunchKernelEx(&cfg, gemm_tc8_kernel, p);
+    cudaError_t r = cudaLaunchKernelEx(&cfg, gemm_tc8_kernel, p);  // GEMM_TC8_THREADS threads
     if (r != cudaSuccess) *e = r;
 }
 

@@ -73,6 +73,7 @@ struct GemmParams {
     int B, npad;                     // slots in the step, MMA N (B rounded up to 16)
     int stages;                      // smem pipeline depth (int8 weights: stages of the int8 + activation ring)
     int stages_b;                    // int8 weights: stages of widened weights in tensor memory
+    int stages_x;                    // int8 weights: stages of the activation ring
     int kbs;                         // int8 weights: k-blocks per stage (1 or 2); fp16 weights: always 2
     int accbufs;                     // TMEM accumulator buffers (1 or 2)
     int prefetch;                    // 1: weights may be fetched before the dependency wait
@@ -94,7 +95,7 @@ size_t gemm_tc_smem_bytes(int npad, int stages);
 // int8-weight GEMM: weights arrive as int8 tiles and are converted to fp16 in
 // shared memory by the epilogue warps before the tensor cores read them.
 void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e);
-size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_a);
+size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_w, int stages_x);
 size_t gemm_tc_stage_bytes(int npad);
 int gemm_tc_max_smem();
 

@@ -387,25 +387,25 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         if (w8) return fail(c, RWKV7_EINVAL, "the CUDA-core GEMM takes fp16 weights only");
         launch_gemm_simt(p, lc, &e);
     } else if (w8) {
-        // Tensor memory: the accumulators and four stages of widened weights
-        // (kbs8 x 32 columns each) in its 512 columns.  Stage q is widened by
-        // converter group q % 4, so with four weight stages each stage slot has
-        // one group, and with a ring A depth that is a multiple of four each
-        // ring A slot's previous stage was waited on by the same group: no
-        // barrier is ever waited on two phases ahead.  One CTA per SM.
+        // Shared memory: ring W (int8 tiles, 8 stages: a multiple of four, see
+        // gemm_tc8_kernel) and ring X (activations) as deep as the rest allows;
+        // tensor memory: the accumulators and four widened weight stages
+        // (kbs8 x 32 columns each) in its 512 columns.  One CTA per SM.
         p.kbs = kbs8;
-        const int SB = 4;
+        const int SB = 4, SW = 8;
         p.accbufs = (2 * p.npad + SB * kbs8 * 32 <= 512) ? 2 : 1;
-        const size_t ab = (size_t)kbs8 * (GEMM_TILE_M * GEMM_TILE_K + (size_t)p.npad * 128);
+        const size_t wb = (size_t)kbs8 * GEMM_TILE_M * GEMM_TILE_K;
+        const size_t xb = (size_t)kbs8 * p.npad * 128;
         const size_t budget = (size_t)gemm_tc_max_smem() - 2048;
-        const int SA = budget / ab >= 8 ? 8 : 4;
-        if (budget / ab < 4 || p.accbufs * p.npad + SB * kbs8 * 32 > 512)
+        const int SX = (int)std::min<size_t>(8, (budget - SW * wb) / xb);
+        if (SX < 2 || p.accbufs * p.npad + SB * kbs8 * 32 > 512)
             return fail(c, RWKV7_ECUDA, "internal: int8 GEMM buffers do not fit");
-        p.stages = SA;
+        p.stages = SW;
         p.stages_b = SB;
-        p.prefetch = nz_skip == nullptr ? 1 : 0;
+        p.stages_x = SX;
+        p.prefetch = 0;  // the int8 producer never waits for the predecessor
         const int grid = std::min(p.nitems, c->nsm);
-        launch_gemm_tc8(p, grid, gemm_tc8_smem_bytes(p.npad, kbs8, SA), lc, &e);
+        launch_gemm_tc8(p, grid, gemm_tc8_smem_bytes(p.npad, kbs8, SW, SX), lc, &e);
     } else {
         // CTAs per SM and pipeline depth: by default one CTA per SM with the
         // deepest pipeline that fits; RWKV7_GEMM_CTAS_PER_SM / RWKV7_GEMM_STAGES
