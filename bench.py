@@ -31,12 +31,14 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 # dram bytes per launch from ncu captures, valid only while the kernel source is
-# unchanged: kernel -> (source file, sha256 prefix of it at capture, workload, bytes)
+# unchanged: kernel -> (source files, sha256 prefix of their concatenation at
+# capture, workload, bytes)
 NCU_TRAFFIC = {
-    ("gemm_tc_kernel", "2.9b"): ("recurrent_decode_gb300/csrc/gemm.cu", "3fb1af53aa13b82e",
+    ("gemm_tc_kernel", "2.9b"): (("recurrent_decode_gb300/csrc/gemm.cu", "recurrent_decode_gb300/csrc/gemm_common.cuh"),
+                                  "4a26b728954c9d79",
                                   "2.9B shape, B=64: DRAM read+write of the 11 GEMM launches of one step of "
                                   "a 2-layer cut (profiles/gemm_traffic_2.9b_b64.md), scaled to 32 layers + head, "
-                                  "per launch", 35823667),
+                                  "per launch", 35823045),
 }
 
 
@@ -49,9 +51,12 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def _sha(path):
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+def _sha(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def class_bytes(dm: synth.Dims, B: int):
@@ -511,7 +516,7 @@ def main():
     traffic = None
     if tr is not None:
         src, sha, _, nbytes = tr
-        if _sha(os.path.join(ROOT, src)) == sha:
+        if _sha([os.path.join(ROOT, f) for f in src]) == sha:
             traffic = nbytes
     sb = step_bytes(dm, B)
     step_gbs = sb / (ms / args.steps / 1e3) / 1e9
