@@ -54,14 +54,15 @@ class TraceStats:
 
 def run_trace(ctx, requests, n_slots: int, decode_prefill_ratio: int = 5, max_prefill_count: int | None = None,
               min_forward_seq_len: int = 10, on_round=None, want_logits: bool = False, abort_at=None,
-              prefix_cache=None) -> TraceStats:
+              prefix_cache=None, device: str = "cuda") -> TraceStats:
     """Run every request to completion (or abort).  on_round(slots, tokens_in, logits,
     next_tokens) is called after each decode round with host int32 arrays (logits: a
     CUDA tensor [B][V] when want_logits, else None).  abort_at: {request index: round}
     -- the request is aborted at the start of that round.  prefix_cache: a
-    PrefixStateCache over slots outside [0, n_slots)."""
+    PrefixStateCache over slots outside [0, n_slots).  device: where the token
+    and slot tensors handed to ctx live (the library takes CUDA tensors)."""
     import torch
-    dev = torch.device("cuda")
+    dev = torch.device(device)
     if max_prefill_count is None:
         max_prefill_count = max(int(n_slots * 0.125), 1)
     abort_at = dict(abort_at or {})
