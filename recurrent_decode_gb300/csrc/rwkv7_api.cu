@@ -500,20 +500,31 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         launch_ln_mix(m, 6, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
-        // G1: r, k, v and the LoRA down projections, as s1 partial slabs
+        // G1: r, k, v and the LoRA down projections, as s1 partial slabs.  Without
+        // a k-split the LoRA-down epilogues apply the activation and write the
+        // fp16 hidden themselves (the LoRA finalize kernel would only convert).
+        const bool fin_fused = s1 == 1;
         Seg g1[7];
         int n1 = 0;
         g1[n1++] = {L_WR, A_XR, c->xmix[0], d, EPI_F32, c->pr, d, nullptr, s1};
         g1[n1++] = {L_WK, A_XK, c->xmix[2], d, EPI_F32, c->pk, d, nullptr, s1};
         g1[n1++] = {L_WV, A_XV, c->xmix[3], d, EPI_F32, c->pv, d, nullptr, s1};
-        g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F32, c->phw, c->rw, nullptr, s1};
-        g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F32, c->pha, c->ra, nullptr, s1};
-        if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F32, c->phv, c->rv, nullptr, s1};
-        g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, s1};
+        if (fin_fused) {
+            g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F16_TANH, c->hw, c->rw, nullptr, 1};
+            g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F16, c->ha, c->ra, nullptr, 1};
+            if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F16, c->hv, c->rv, nullptr, 1};
+            g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F16_SIGMOID, c->hg, c->rg, nullptr, 1};
+        } else {
+            g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F32, c->phw, c->rw, nullptr, s1};
+            g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F32, c->pha, c->ra, nullptr, s1};
+            if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F32, c->phv, c->rv, nullptr, s1};
+            g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, s1};
+        }
         pb(P_GEMM_PROJ);
         if ((rc = run_gemm(c, l, g1, n1, B, nullptr, nullptr, lc, mode))) return rc;
         pe();
         // LoRA down: add the slabs, activation, fp16 (the LoRA-up GEMM's operands)
+        if (!fin_fused) {
         LoraFinParams lf;
         memset(&lf, 0, sizeof lf);
         lf.B = B;
@@ -527,6 +538,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         launch_lora_fin(lf, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "lora_fin launch: %s", cudaGetErrorString(e));
+        }
         // G2: LoRA up projections with their gates
         Seg g2[4];
         int n2 = 0;
@@ -1576,7 +1588,10 @@ int rwkv7_set_mode(rwkv7_ctx *c, int32_t mode) {
 int32_t rwkv7_step_kernel_count(const rwkv7_ctx *c, int32_t B, int32_t with_sampling) {
     if (!c || B < 1) return 0;
     const int sub = (B + MAX_B - 1) / MAX_B;
-    return sub * (1 + 9 * c->L + 2 + (with_sampling ? 1 : 0));
+    int s1, s3, s5;
+    step_splits(c, &s1, &s3, &s5);
+    const int per_layer = s1 == 1 ? 8 : 9;  // the LoRA finalize kernel runs only for a split r, k, v GEMM
+    return sub * (1 + per_layer * c->L + 2 + (with_sampling ? 1 : 0));
 }
 
 int rwkv7_ffn_union_stats(rwkv7_ctx *c, uint64_t *nonzero_blocks, uint64_t *blocks) {
