@@ -161,7 +161,7 @@ RWKV7_API int rwkv7_sample_batch(rwkv7_ctx *ctx, const int32_t *d_slots, const f
  * (16 MiB), e.g. 64 rows of a 65,536-token vocabulary. */
 #define RWKV7_SAMPLE_STATIC_MAX_ELEMS (1 << 22)
 
-/* Allocation-free variant of rwkv7_sample_batch.  The paper has no counterpart:
+/* Allocation-free variant of rwkv7_sample_batch.  The articles describe no counterpart:
  * it is a library convenience for callers that must not allocate device memory
  * while they sample -- a serving process that has already handed all of HBM to
  * its own arena (so cudaMalloc would fail), or a loop that cannot afford the
