@@ -68,3 +68,11 @@ def test_int8_weights_spread_like_fp16_variant():
     q, sc = i8["blocks.0.att.key"]
     w = q.astype(np.float64) * sc.astype(np.float64)[:, None]
     assert 0.015 < w.std() < 0.025 and q.min() >= -127 and q.max() <= 127
+
+
+def test_int8_weights_independent_of_thread_count():
+    a16, a8 = synth.make_weights_i8("0.1b", threads=1, n_layer=1)
+    b16, b8 = synth.make_weights_i8("0.1b", threads=8, n_layer=1)
+    assert a16.keys() == b16.keys() and a8.keys() == b8.keys()
+    assert all(np.array_equal(a16[k], b16[k]) for k in a16)
+    assert all(np.array_equal(a8[k][0], b8[k][0]) and np.array_equal(a8[k][1], b8[k][1]) for k in a8)
