@@ -129,3 +129,98 @@ def test_draw_stream_depends_on_seed_and_index():
     a = [oracle.draw_u64(1000, i) for i in range(4)]
     b = [oracle.draw_u64(1001, i) for i in range(4)]
     assert len(set(a)) == 4 and not set(a) & set(b)
+
+
+def _kept_by_definition(q1, top_p, top_k):
+    """The kept set written out from the reading of the worker's per-slot top_p /
+    top_k (RWKV-Runner Albatross page, worker main loop): the top-p set is every
+    token whose T=1 weight is at least the cut value, the cut being the largest
+    weight value whose class and every heavier class together hold at least
+    ceil(top_p * total) (at least 1, at most the total); then top-k keeps the
+    first k tokens of the order (weight descending, index ascending); the result
+    is the intersection.  Plain loops over the integer weights."""
+    q = [int(x) for x in q1]
+    total = sum(q)
+    target = min(max(1, math.ceil(float(np.float32(top_p)) * total)), total)
+    mass_at = {}
+    for x in q:
+        mass_at[x] = mass_at.get(x, 0) + x
+    acc, cut = 0, None
+    for val in sorted(mass_at, reverse=True):
+        acc += mass_at[val]
+        if acc >= target:
+            cut = val
+            break
+    keep = [x >= cut for x in q]
+    if 0 < top_k < len(q):
+        order = sorted(range(len(q)), key=lambda i: (-q[i], i))
+        allowed = set(order[:top_k])
+        keep = [keep[i] and i in allowed for i in range(len(q))]
+    return np.array(keep)
+
+
+def _tied_logits(V, seed, n_levels):
+    """Logits drawn from a few distinct values, so that ties fall at the top-k
+    boundary and at the top-p cut."""
+    g = np.random.default_rng(seed)
+    levels = np.sort(g.normal(0, 1.5, n_levels)).astype(np.float32)
+    return levels[g.integers(0, n_levels, V)].astype(np.float32)
+
+
+@pytest.mark.parametrize("V", [16, 257, 4096])
+@pytest.mark.parametrize("top_p", [0.05, 0.3, 0.9, 1.0])
+@pytest.mark.parametrize("top_k", [2, 5, 20, 200])
+def test_top_k_intersect_top_p_matches_definition(V, top_p, top_k):
+    """top-k > 1 together with top-p: the oracle's kept set equals the set built
+    from the definition, on continuous logits, on logits with many exact ties,
+    and with a penalty in effect (the integer weights then come from the
+    penalised logits)."""
+    cases = [(_logits(V, 100 + V + top_k), np.zeros(V, np.float32)),
+             (_tied_logits(V, 200 + V + top_k, 5), np.zeros(V, np.float32)),
+             (_tied_logits(V, 300 + V + top_k, 17), np.zeros(V, np.float32))]
+    g = np.random.default_rng(V * 7 + top_k)
+    occ = np.where(g.uniform(size=V) < 0.2, g.integers(1, 4, V), 0).astype(np.float32)
+    cases.append((_logits(V, 400 + V + top_k, scale=1.0), occ))
+    for lg, oc in cases:
+        params = dict(top_p=top_p, top_k=top_k, temperature=1.0, presence=0.3, frequency=0.5)
+        q1, qT, kept = oracle.sample_weights(lg, oc, params)
+        want = _kept_by_definition(q1, top_p, top_k)
+        assert np.array_equal(kept, want)
+        assert kept.sum() <= top_k
+        assert np.all(qT[~kept] == 0) and np.all(qT[kept] == q1[kept])
+
+
+def test_top_k_boundary_ties_keep_lowest_indices():
+    """Equal weights straddling the k-th place: the lower indices are kept, and
+    the set size is exactly k when the top-p set holds at least k tokens."""
+    lg = np.zeros(12, np.float32)
+    lg[[2, 5, 8, 11]] = 1.0  # four tokens tie for the top
+    for k in (1, 2, 3, 4):
+        _, _, kept = oracle.sample_weights(lg, np.zeros(12, np.float32), dict(top_p=1.0, top_k=k))
+        assert list(np.flatnonzero(kept)) == [2, 5, 8, 11][:k]
+    _, _, kept = oracle.sample_weights(lg, np.zeros(12, np.float32), dict(top_p=1.0, top_k=6))
+    assert list(np.flatnonzero(kept)) == [0, 1, 2, 5, 8, 11]
+
+
+def test_top_p_mass_is_taken_over_the_whole_vocabulary():
+    """The top-p cut is computed on all tokens, before top-k: with a long flat
+    tail, top_p = 0.9 keeps many tokens, so top-k = 3 keeps three of them.  (If
+    the mass were taken over the top-k tokens only, a dominant first token would
+    be kept alone.)"""
+    V = 64
+    lg = np.full(V, -1.0, np.float32)
+    lg[0] = 3.0
+    _, _, kept = oracle.sample_weights(lg, np.zeros(V, np.float32), dict(top_p=0.9, top_k=3))
+    assert list(np.flatnonzero(kept)) == [0, 1, 2]
+    _, _, kept_p = oracle.sample_weights(lg, np.zeros(V, np.float32), dict(top_p=0.3, top_k=3))
+    assert list(np.flatnonzero(kept_p)) == [0]
+
+
+def test_sample_draws_only_from_the_top_k_top_p_set():
+    V = 1024
+    lg = _tied_logits(V, 55, 9)
+    params = dict(top_p=0.6, top_k=20, temperature=0.8, seed=5, penalty_decay=1.0)
+    _, _, kept = oracle.sample_weights(lg, np.zeros(V, np.float32), params)
+    for i in range(300):
+        tok, kk = oracle.sample(lg, np.zeros(V, np.float32), params, i)
+        assert kept[tok] and np.array_equal(kk, kept)
