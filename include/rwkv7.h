@@ -93,6 +93,19 @@ RWKV7_API int rwkv7_create_ex(const rwkv7_config *cfg, int32_t weight_bits, void
 /* 16 or 8 (see rwkv7_create_ex); 0 for NULL. */
 RWKV7_API int32_t rwkv7_weight_bits(const rwkv7_ctx *ctx);
 
+/* Device allocator hook.  A context created after this call takes every
+ * device allocation of its lifetime (weights, slot pool, scratch) from
+ * alloc(user, bytes, &ptr) -- which returns 0 and a 256-byte aligned device
+ * pointer on success, anything else on failure -- and hands each back to
+ * release(user, ptr) in rwkv7_destroy, so a serving process can place the
+ * library's memory in its own pool.  Both NULL restores cudaMalloc / cudaFree;
+ * only one NULL returns RWKV7_EINVAL.  A refused allocation makes the creating
+ * call return RWKV7_ENOMEM with the ctx still destroyable.  Process-wide;
+ * contexts already created keep the allocator they were created with. */
+typedef int (*rwkv7_alloc_fn)(void *user, size_t bytes, void **d_ptr);
+typedef void (*rwkv7_free_fn)(void *user, void *d_ptr);
+RWKV7_API int rwkv7_set_device_allocator(rwkv7_alloc_fn alloc, rwkv7_free_fn release, void *user);
+
 /* Free everything the ctx owns (synchronizes its stream first).  NULL is a no-op. */
 RWKV7_API void rwkv7_destroy(rwkv7_ctx *ctx);
 
@@ -116,16 +129,30 @@ RWKV7_API int rwkv7_set_weight_i8(rwkv7_ctx *ctx, const char *name, const int8_t
  * fp16 data) and set it.  Synchronous. */
 RWKV7_API int rwkv7_load_weights(rwkv7_ctx *ctx, const char *path);
 
-/* Slot pool (the Albatross worker keeps one state slot per active sequence and
+/* Slot pool (RWKV-Runner Albatross article, "策略语法与参数解析": the worker
+ * keeps real_state_size = batch_size state slots, one per active sequence, and
  * swaps slots when it reorganises the batch; here slots are addressed by index,
- * so reorganising needs no copies).  Stream-ordered. */
+ * so reorganising needs no copies).  Slots run from 0 to n_slots - 1; an index
+ * outside that range returns RWKV7_EINVAL.  Stream-ordered. */
 RWKV7_API int rwkv7_slot_reset(rwkv7_ctx *ctx, int32_t slot);            /* zero state, occurrence counts, draw counter */
 RWKV7_API int rwkv7_slot_swap(rwkv7_ctx *ctx, int32_t a, int32_t b);     /* exchange everything two slots hold */
-RWKV7_API int rwkv7_slot_copy(rwkv7_ctx *ctx, int32_t src, int32_t dst); /* dst := src (prefix-state reuse) */
+/* dst := src (recurrent and shift states; dst's occurrence counts and draw
+ * counter restart).  The article's roadmap ("边界与后续路线") names a prefix
+ * state cache, first as an in-memory LRU; this copy is its building block. */
+RWKV7_API int rwkv7_slot_copy(rwkv7_ctx *ctx, int32_t src, int32_t dst);
+/* Per-slot sampling parameters, kept in the pool (the Albatross worker holds
+ * per-slot temperature / top_p / top_k / penalty tensors pre-allocated on the
+ * device, "连续批处理Worker 主循环"; its adapter's defaults are listed with
+ * rwkv7_sampling).  Copied from host memory; stream-ordered. */
 RWKV7_API int rwkv7_slot_set_sampling(rwkv7_ctx *ctx, int32_t slot, const rwkv7_sampling *params);
 
-/* Checkpoint of one slot's recurrent state: fp32 wkv [L][H][64][64], then fp32
- * token-shift states of the time mix [L][d] and of the channel mix [L][d]. */
+/* Checkpoint of one slot's recurrent state -- the per-sequence state tuple
+ * (shift_state, wkv_state) that the RWKV-Server article's prefill hands to the
+ * model ("RWKV 批量推理中 Prefill 的正确打开方式", §五, the prefill method of
+ * task.py) -- as fp32 wkv [L][H][64][64], then fp32 token-shift states of the
+ * time mix [L][d] and of the channel mix [L][d].  host_buf is a caller-owned
+ * HOST buffer of exactly rwkv7_slot_state_bytes() bytes (RWKV7_EINVAL
+ * otherwise).  Both calls synchronize the ctx stream. */
 RWKV7_API size_t rwkv7_slot_state_bytes(const rwkv7_ctx *ctx);
 RWKV7_API int rwkv7_slot_get_state(rwkv7_ctx *ctx, int32_t slot, void *host_buf, size_t bytes);
 RWKV7_API int rwkv7_slot_set_state(rwkv7_ctx *ctx, int32_t slot, const void *host_buf, size_t bytes);
@@ -138,11 +165,18 @@ RWKV7_API int rwkv7_slot_set_state(rwkv7_ctx *ctx, int32_t slot, const void *hos
 RWKV7_API int rwkv7_prefill_seq(rwkv7_ctx *ctx, int32_t slot, const int32_t *d_tokens, int32_t T,
                       float *d_logits_out);
 
-/* One decode step of B slots: slot d_slots[b] consumes token d_tokens[b]
- * (device int32 [B] each; slots distinct, 1 <= B <= n_slots).  Writes fp32
- * logits [B][V] to d_logits_out if not NULL, and if d_next_out is not NULL
- * samples the next token of every slot with its sampling parameters (updating
- * its occurrence counts and draw counter) into d_next_out [B]. */
+/* One decode step of B slots -- the Albatross worker's per-round
+ * forward_seq_batch over the organised slot batch followed by its penalties and
+ * sample_next_tokens_batch (RWKV-Runner article, "连续批处理Worker 主循环"), the
+ * B > 1, T = 1 path of the RWKV-Server article ("RWKV 批量推理中 Prefill 的正确打开方式",
+ * §三): slot d_slots[b] consumes token d_tokens[b] (device int32 [B] each;
+ * slots distinct, 1 <= B <= n_slots; B > 256 runs as consecutive fused steps).
+ * Writes fp32 logits [B][V] to d_logits_out if not NULL, and if d_next_out is
+ * not NULL samples the next token of every slot with its sampling parameters
+ * (updating its occurrence counts and draw counter) into d_next_out [B].
+ * Returns RWKV7_EINVAL for null inputs or B out of range, RWKV7_ESTATE before
+ * every weight is set; bad slot or token values are latched on the device and
+ * reported by rwkv7_synchronize.  Asynchronous on the ctx stream. */
 RWKV7_API int rwkv7_decode_step(rwkv7_ctx *ctx, const int32_t *d_slots, const int32_t *d_tokens,
                       int32_t B, float *d_logits_out, int32_t *d_next_out);
 
@@ -152,8 +186,13 @@ RWKV7_API int rwkv7_decode_step(rwkv7_ctx *ctx, const int32_t *d_slots, const in
 RWKV7_API int rwkv7_decode_step_host(rwkv7_ctx *ctx, const int32_t *h_slots, const int32_t *h_tokens,
                            int32_t B, float *h_logits_out, int32_t *h_next_out);
 
-/* Sample one token per slot from caller logits (device fp32 [B][V]) with the
- * slots' sampling parameters; updates occurrence counts and draw counters. */
+/* Sample one token per slot from caller logits (device fp32 [B][V], row b for
+ * slot d_slots[b]) with the slots' sampling parameters -- the worker's batched
+ * sample_next_tokens_batch with per-slot top_k / top_p / temperature and the
+ * presence / frequency penalties applied first (RWKV-Runner article,
+ * "连续批处理Worker 主循环"; defaults from "适配器Runner 与异步引擎之间的桥").
+ * Updates the slots' occurrence counts and draw counters; writes d_next_out
+ * [B].  RWKV7_EINVAL for null pointers or B out of range.  Asynchronous. */
 RWKV7_API int rwkv7_sample_batch(rwkv7_ctx *ctx, const int32_t *d_slots, const float *d_logits,
                        int32_t B, int32_t *d_next_out);
 
@@ -215,9 +254,19 @@ RWKV7_API int rwkv7_sample_rows_static(const float *d_logits, const int32_t *d_r
  * wait that gave up).  Clears the latched error. */
 RWKV7_API int rwkv7_synchronize(rwkv7_ctx *ctx);
 
+/* Test hook: OR `flags` (bits of the device error word: 1 bad slot, 2 bad
+ * token, 4 repeated slot, 8 a bounded in-kernel wait gave up, 16 sampler
+ * found no token) into the ctx's device error word, as a kernel would latch
+ * it, so that the error path of rwkv7_synchronize can be exercised without
+ * making any kernel fail.  Synchronizes the ctx stream. */
+RWKV7_API int rwkv7_debug_latch_error(rwkv7_ctx *ctx, uint32_t flags);
+
 /* Select the decode implementation: 0 = tensor-core kernels with CUDA-graph
  * replay (default), 1 = the same kernels launched directly, 2 = CUDA-core
- * (SIMT) projection kernels launched directly (a slow cross-check). */
+ * (SIMT) projection kernels launched directly (a slow cross-check), 3 = one
+ * persistent cooperative kernel for the whole step (B <= 256; correct, and
+ * slower than mode 0 today).  Modes 2 and 3 take fp16 weights only.
+ * RWKV7_EINVAL for another value. */
 RWKV7_API int rwkv7_set_mode(rwkv7_ctx *ctx, int32_t mode);
 
 /* The ctx's own device I/O buffers for a fused step (capacity min(n_slots, 256)
@@ -258,6 +307,21 @@ RWKV7_API int rwkv7_ffn_union_stats(rwkv7_ctx *ctx, uint64_t *nonzero_blocks, ui
 RWKV7_API int rwkv7_profile_step(rwkv7_ctx *ctx, const int32_t *d_slots, const int32_t *d_tokens,
                                  int32_t B, int32_t with_sampling, float *ms_out,
                                  int32_t *launches_out, int32_t n_classes);
+
+/* In-graph timeline of one decode step of B <= min(n_slots, 256) slots (with
+ * logits, and with sampling if with_sampling != 0), for measurement: the step
+ * runs as the same CUDA graph the decode path replays (mode 0; mode 1 launches
+ * it directly), every kernel stamping the GPU's global nanosecond timer.  For
+ * launch i (in launch order) host_times[4*i .. 4*i+3] receive the earliest CTA
+ * start, the earliest and the latest return of a CTA from its wait for the
+ * preceding kernel, and the latest CTA end; host_classes[i] its
+ * RWKV7_PROF_* class; *n_launches the number of launches (at most
+ * max_launches).  The end of launch i minus the end of launch i - 1 is the time
+ * that launch adds to the step.  The step is a real step: the slots' states
+ * advance.  Synchronous; RWKV7_EINVAL for bad arguments or mode 2 / 3. */
+RWKV7_API int rwkv7_step_timeline(rwkv7_ctx *ctx, const int32_t *d_slots, const int32_t *d_tokens, int32_t B,
+                                  int32_t with_sampling, uint64_t *host_times, int32_t *host_classes,
+                                  int32_t max_launches, int32_t *n_launches);
 
 /* Number of kernels one decode step of B slots launches (with / without
  * sampling), for launch accounting. */

@@ -41,6 +41,8 @@ class Sampling(C.Structure):
 
 # name -> (restype, argtypes): the whole exported ABI
 _VP, _I32P, _FP = C.c_void_p, C.POINTER(C.c_int32), C.c_void_p
+ALLOC_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_size_t, C.POINTER(C.c_void_p))
+FREE_FN = C.CFUNCTYPE(None, C.c_void_p, C.c_void_p)
 SIGNATURES = {
     "rwkv7_create": (C.c_int, [C.POINTER(Config), C.c_void_p, C.POINTER(C.c_void_p)]),
     "rwkv7_create_ex": (C.c_int, [C.POINTER(Config), C.c_int32, C.c_void_p, C.POINTER(C.c_void_p)]),
@@ -72,6 +74,10 @@ SIGNATURES = {
     "rwkv7_step_kernel_count": (C.c_int32, [_VP, C.c_int32, C.c_int32]),
     "rwkv7_profile_step": (C.c_int, [_VP, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
                                      C.c_void_p, C.c_int32]),
+    "rwkv7_set_device_allocator": (C.c_int, [ALLOC_FN, FREE_FN, C.c_void_p]),
+    "rwkv7_debug_latch_error": (C.c_int, [_VP, C.c_uint32]),
+    "rwkv7_step_timeline": (C.c_int, [_VP, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
+                                      C.c_void_p, C.c_int32, C.POINTER(C.c_int32)]),
 }
 
 SAMPLE_STATIC_MAX_ELEMS = 1 << 22
@@ -148,6 +154,37 @@ def sample_rows_static(logits, rows, occ, params, ndraw, next_out, err, stream=N
                                       _ptr(err, torch.int32, "err"), C.c_void_p(st.cuda_stream), C.byref(msg))
     if rc != OK:
         raise RWKV7Error(rc, (msg.value or b"").decode())
+
+
+_allocator_refs = None  # keeps the installed ctypes callbacks alive
+
+
+def set_device_allocator(alloc=None, free=None):
+    """rwkv7_set_device_allocator: contexts created from now on take their device
+    memory from alloc(nbytes) -> device address (int; 0 or an exception refuses)
+    and return it through free(address).  No arguments restores cudaMalloc."""
+    global _allocator_refs
+    lib = load_library()
+    if alloc is None and free is None:
+        rc = lib.rwkv7_set_device_allocator(ALLOC_FN(), FREE_FN(), None)
+        _allocator_refs = None
+    else:
+        def _a(_user, nbytes, out):
+            try:
+                p = int(alloc(int(nbytes)) or 0)
+            except Exception:
+                p = 0
+            out[0] = p or None
+            return 0 if p else 1
+
+        def _f(_user, ptr):
+            free(int(ptr or 0))
+        refs = (ALLOC_FN(_a), FREE_FN(_f))
+        rc = lib.rwkv7_set_device_allocator(refs[0], refs[1], None)
+        if rc == OK:
+            _allocator_refs = refs
+    if rc != OK:
+        raise RWKV7Error(rc, "alloc and free must both be given or both omitted")
 
 
 class Rwkv7:
@@ -292,6 +329,10 @@ class Rwkv7:
     def synchronize(self):
         self._check(self.lib.rwkv7_synchronize(self.h))
 
+    def debug_latch_error(self, flags: int):
+        """Test hook: OR flags into the device error word (rwkv7_debug_latch_error)."""
+        self._check(self.lib.rwkv7_debug_latch_error(self.h, int(flags)))
+
     def set_mode(self, mode: int):
         self._check(self.lib.rwkv7_set_mode(self.h, mode))
 
@@ -309,6 +350,22 @@ class Rwkv7:
                                                 int(bool(with_sampling)), ms.ctypes.data, cnt.ctypes.data, n))
         return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(PROF_CLASSES)}
 
+    def step_timeline(self, slots, tokens, with_sampling: bool = False, max_launches: int = 4096):
+        """rwkv7_step_timeline: one graph-replayed step with every kernel stamping
+        the GPU timer.  Returns (times [n, 4] int64 ns -- earliest start, earliest
+        and latest dependency release, latest end of each launch -- and the
+        class name of each launch)."""
+        import torch
+        t = np.zeros((max_launches, 4), np.uint64)
+        cls = np.zeros(max_launches, np.int32)
+        n = C.c_int32()
+        self._check(self.lib.rwkv7_step_timeline(self.h, _ptr(slots, torch.int32, "slots"),
+                                                 _ptr(tokens, torch.int32, "tokens"), slots.numel(),
+                                                 int(bool(with_sampling)), t.ctypes.data, cls.ctypes.data,
+                                                 max_launches, C.byref(n)))
+        k = int(n.value)
+        return t[:k].astype(np.int64), [PROF_CLASSES[c] for c in cls[:k]]
+
     def io_buffers(self):
         """(slots, tokens, logits, next) device pointers owned by the context."""
         p = [C.c_void_p() for _ in range(4)]
@@ -317,4 +374,4 @@ class Rwkv7:
 
 
 __all__ = ["Rwkv7", "RWKV7Error", "Config", "Sampling", "load_library", "build", "LIB_PATH",
-           "SIGNATURES", "MAX_STEP_BATCH", "PROF_CLASSES"]
+           "SIGNATURES", "MAX_STEP_BATCH", "PROF_CLASSES", "set_device_allocator"]

@@ -127,8 +127,10 @@ __device__ __forceinline__ void ln8(float (&v)[8], bool act, int d, const uint4 
 __global__ void embed_kernel(const ElemParams p) {
     extern __shared__ uint32_t bitmap[];
     __shared__ float red[64];
+    if (threadIdx.x == 0) tl_start(p.tl);
     pdl_wait();
     pdl_launch();
+    if (threadIdx.x == 0) tl_release(p.tl);
     const int b = blockIdx.x;
     const int i0 = threadIdx.x * 8;
     const bool act = i0 < p.d;
@@ -148,6 +150,7 @@ __global__ void embed_kernel(const ElemParams p) {
     }
     ln8(v, act, p.d, w4, b4, red);
     if (act) st8f(p.x + (size_t)b * p.d + i0, v);
+    if (threadIdx.x == 0) tl_end(p.tl);
     if (b == 0 && p.single_slot < 0) {
         const int words = (p.n_slots + 31) / 32;
         for (int i = threadIdx.x; i < words; i += blockDim.x) bitmap[i] = 0u;
@@ -169,6 +172,7 @@ __global__ void embed_kernel(const ElemParams p) {
 template <int NMIX>
 __global__ void ln_mix_kernel(const ElemParams p) {
     __shared__ float red[64];
+    if (threadIdx.x == 0) tl_start(p.tl);
     const int b = blockIdx.x;
     const int i0 = threadIdx.x * 8;
     const bool act = i0 < p.d;
@@ -186,6 +190,7 @@ __global__ void ln_mix_kernel(const ElemParams p) {
     }
     pdl_wait();
     pdl_launch();
+    if (threadIdx.x == 0) tl_release(p.tl);
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (act) {
         ld8f(p.x + (size_t)b * p.d + i0, v);
@@ -205,11 +210,13 @@ __global__ void ln_mix_kernel(const ElemParams p) {
         *reinterpret_cast<uint4 *>(p.xo[q] + (size_t)b * p.d + i0) = f_to_h8(o);
     }
     if (ok) st8f(shp, v);
+    if (threadIdx.x == 0) tl_end(p.tl);
 }
 
 // xo[0][b] = fp16(LN_out(x[b])): the input of the head projection.
 __global__ void ln_out_kernel(const ElemParams p) {
     __shared__ float red[64];
+    if (threadIdx.x == 0) tl_start(p.tl);
     const int b = blockIdx.x;
     const int i0 = threadIdx.x * 8;
     const bool act = i0 < p.d;
@@ -220,6 +227,7 @@ __global__ void ln_out_kernel(const ElemParams p) {
     }
     pdl_wait();
     pdl_launch();
+    if (threadIdx.x == 0) tl_release(p.tl);
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (act) {
         ld8f(p.x + (size_t)b * p.d + i0, v);
@@ -227,6 +235,7 @@ __global__ void ln_out_kernel(const ElemParams p) {
     }
     ln8(v, act, p.d, w4, b4, red);
     if (act) *reinterpret_cast<uint4 *>(p.xo[0] + (size_t)b * p.d + i0) = f_to_h8(v);
+    if (threadIdx.x == 0) tl_end(p.tl);
 }
 
 static int ln_threads(int d) { return ((d / 8) + 31) / 32 * 32; }
@@ -277,6 +286,7 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
     const bool ok = slot >= 0 && slot < p.n_slots;
     float *S = p.wkv + ((size_t)(ok ? slot : 0) * p.H + h) * (HS * HS);
     if (tid == 0) {
+        tl_start(p.tl);
         sm.ok = 0u;
         mbar_init(&sm.full, 1);
         fence_barrier_init();
@@ -285,6 +295,7 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
     }
     pdl_wait();
     pdl_launch();
+    if (tid == 0) tl_release(p.tl);
 
     const size_t off = (size_t)b * p.d + (size_t)h * HS;
     float rv = 0.f, kpv = 0.f, vpv = 0.f;
@@ -362,6 +373,7 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
         const float yn = dv * (1.0f / sqrtf(var + 64e-5f)) * __half2float(p.lnx_w[c]) + __half2float(p.lnx_b[c]);
         const float bonus = sum64(rv * kpv * __half2float(p.r_k[c]), sm.red, 1);
         p.z[off + tid] = __float2half_rn((yn + bonus * vpv) * p.g[off + tid]);
+        if (tid == 0) tl_end(p.tl);
     }
 }
 
@@ -581,8 +593,10 @@ __global__ void __launch_bounds__(64) wkv_gate_kernel(const WkvSeqParams p) {
 // S partial slabs, passed through the LoRA's activation and rounded to fp16.
 __global__ void lora_fin_kernel(const LoraFinParams p) {
     const int b = blockIdx.x;
+    if (threadIdx.x == 0) tl_start(p.tl);
     pdl_wait();
     pdl_launch();
+    if (threadIdx.x == 0) tl_release(p.tl);
     const int total = p.r[0] + p.r[1] + p.r[2] + p.r[3];
     for (int c = threadIdx.x; c < total; c += blockDim.x) {
         int i = 0, col = c;
@@ -597,6 +611,7 @@ __global__ void lora_fin_kernel(const LoraFinParams p) {
         const float y = p.act[i] == 1 ? fast_tanh(acc) : (p.act[i] == 2 ? fast_sigmoid(acc) : acc);
         p.out[i][(size_t)b * p.r[i] + col] = __float2half_rn(y);
     }
+    if (threadIdx.x == 0) tl_end(p.tl);
 }
 
 // ---------------------------------------------------------------------------

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int i_begin = item_first(c, G, nitems), i_end = item_first(c + 1, G, nitems);
+    if (threadIdx.x == 0) tl_start(p.tl);
     uint32_t ncols = 32;
     while ((int)ncols < NB * npad) ncols <<= 1;
 
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             const uint64_t polW = policy_evict_first(), polX = policy_evict_last();
             pdl_wait();
             pdl_launch();
+            tl_release(p.tl);
             bool ok = true;
             if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
             int q = 0;  // stage sequence number
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
     __syncwarp();  // warps 0 and 1 reconverge (lane 0 ran the producer / MMA loop)
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) tl_end(p.tl);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, ncols);
@@ -308,8 +311,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
     const int blk = local / sg.S, split = local % sg.S;
     const int kb0 = (int)(((long long)split * sg.kb) / sg.S), kb1 = (int)(((long long)(split + 1) * sg.kb) / sg.S);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) tl_start(p.tl);
     pdl_wait();
     pdl_launch();
+    if (threadIdx.x == 0) tl_release(p.tl);
     bool nzany = false;
     for (int rr = 0; rr < 8; ++rr) {
         const int n = blk * 64 + warp * 8 + rr;
@@ -369,6 +374,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
             if (p.nz_count && f) atomicAdd(p.nz_count, 1ull);
         }
     }
+    __syncthreads();
+    if (threadIdx.x == 0) tl_end(p.tl);
 }
 
 void launch_gemm_simt(const GemmParams &p, const LaunchCfg &lc, cudaError_t *e) {

@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(GEMM_TC8_THREADS, 1) gemm_tc8_kernel(const __g
     uint32_t *nzf = tmem_slot + 2;  // [2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) tl_start(p.tl);
     const int G = gridDim.x, c = blockIdx.x;
     const int i_begin = item_first(c, G, nitems), i_end = item_first(c + 1, G, nitems);
     const uint32_t ncols = 512;                        // accumulators + widened weight stages
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(GEMM_TC8_THREADS, 1) gemm_tc8_kernel(const __g
             const uint64_t polX = policy_evict_last();
             pdl_wait();
             pdl_launch();
+            tl_release(p.tl);
             bool ok = true;
             if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
             int q = 0;
@@ -364,6 +366,7 @@ __global__ void __launch_bounds__(GEMM_TC8_THREADS, 1) gemm_tc8_kernel(const __g
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) tl_end(p.tl);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, ncols);

@@ -81,6 +81,7 @@ struct GemmParams {
     unsigned long long *nz_count;    // EPI_RELU2: running count of nonzero 64-row blocks (or null)
     const uint32_t *nz_skip;         // nonzero flags per k-block of the activations (or null)
     uint32_t *err;
+    unsigned long long *tl;          // timeline words of this launch (measurement only; else null)
 };
 
 // Launch helpers (implemented in the .cu files).
@@ -114,6 +115,7 @@ struct ElemParams {
     uint32_t *err;
     int single_slot;          // prefill: every row is a token of this slot (-1: rows are slots)
     float *xout;              // prefill: residual after the slab adds (x is read only)
+    unsigned long long *tl;   // timeline words of this launch (measurement only; else null)
 };
 
 void launch_embed(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e);
@@ -158,6 +160,7 @@ struct WkvParams {
     float *wkv;                      // this layer's states [n_slots][H][64][64]
     __half *z;                       // [B][d]
     uint32_t *err;
+    unsigned long long *tl;          // timeline words of this launch (measurement only; else null)
 };
 void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e);
 
@@ -169,6 +172,7 @@ struct LoraFinParams {
     int act[4];
     const float *part[4];  // [S][bcap][r]
     __half *out[4];        // [B][r]
+    unsigned long long *tl;  // timeline words of this launch (measurement only; else null)
 };
 void launch_lora_fin(const LoraFinParams &p, const LaunchCfg &lc, cudaError_t *e);
 
@@ -254,6 +258,7 @@ struct SamplerParams {
     float *lpen;           // scratch [B][V]
     int32_t *next;         // [B]
     uint32_t *err;
+    unsigned long long *tl;  // timeline words of this launch (measurement only; else null)
 };
 void launch_sampler(const SamplerParams &p, const LaunchCfg &lc, cudaError_t *e);
 
@@ -286,6 +291,24 @@ __device__ __forceinline__ uint64_t gtimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// In-graph timeline of a step (a measurement aid; the pointer is null in normal
+// steps).  Each launch owns four %globaltimer words: the earliest CTA start,
+// the earliest and latest return from the dependency wait, the latest CTA end.
+// Start words are preset to all ones, the others to zero.
+__device__ __forceinline__ void tl_start(unsigned long long *tl) {
+    if (tl) atomicMin(tl, (unsigned long long)gtimer());
+}
+__device__ __forceinline__ void tl_release(unsigned long long *tl) {
+    if (tl) {
+        const unsigned long long t = gtimer();
+        atomicMin(tl + 1, t);
+        atomicMax(tl + 2, t);
+    }
+}
+__device__ __forceinline__ void tl_end(unsigned long long *tl) {
+    if (tl) atomicMax(tl + 3, (unsigned long long)gtimer());
 }
 
 // Programmatic dependent launch: wait for the preceding grid's completion (and

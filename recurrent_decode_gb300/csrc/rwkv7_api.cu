@@ -19,6 +19,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -61,6 +62,16 @@ struct Prof {
 
 // activation buffers addressed by tensor maps
 enum ABuf { A_XR, A_XW, A_XK, A_XV, A_XA, A_XG, A_HW, A_HA, A_HV, A_HG, A_Z, A_XKF, A_H, A_XO, A_COUNT };
+
+// Device allocator for contexts created from now on (rwkv7_set_device_allocator);
+// both null: cudaMalloc / cudaFree.
+struct DevAllocator {
+    rwkv7_alloc_fn alloc = nullptr;
+    rwkv7_free_fn release = nullptr;
+    void *user = nullptr;
+};
+std::mutex g_alloc_mu;
+DevAllocator g_alloc;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -135,7 +146,11 @@ struct rwkv7_ctx {
     void *abase[A_COUNT]{};
     int acols[A_COUNT]{};
 
-    std::map<std::tuple<int, int, int, int>, cudaGraphExec_t> graphs;
+    std::map<std::tuple<int, int, int, int, int>, cudaGraphExec_t> graphs;
+    // in-graph timeline (rwkv7_step_timeline): four words per launch, and the
+    // kernel class of each launch of the captured step
+    unsigned long long *tlbuf = nullptr;
+    std::map<std::tuple<int, int, int>, std::vector<int>> tl_classes;
     // persistent step: counters (phase, tile, slot bitmap, abort), zeroed per step
     uint32_t *pkbuf = nullptr;
     size_t pk_words = 0;
@@ -143,6 +158,7 @@ struct rwkv7_ctx {
     float *p4 = nullptr;  // key-projection partial slabs [PK_S4_MAX][bcap][F]
     std::map<std::pair<int, int>, PkParams> pk_params;
     std::vector<void *> allocs;
+    DevAllocator alloc;  // the allocator in effect when the ctx was created
     Prof prof;
 };
 
@@ -169,10 +185,21 @@ int fail(rwkv7_ctx *c, int code, const char *fmt, ...) {
 template <typename T>
 int dalloc(rwkv7_ctx *c, T **p, size_t count) {
     void *q = nullptr;
-    cudaError_t e = cudaMalloc(&q, count * sizeof(T) + 256);
-    if (e != cudaSuccess) return fail(c, RWKV7_ENOMEM, "cudaMalloc(%zu bytes): %s", count * sizeof(T), cudaGetErrorString(e));
+    const size_t bytes = count * sizeof(T) + 256;
+    if (c->alloc.alloc) {
+        if (c->alloc.alloc(c->alloc.user, bytes, &q) != 0 || !q)
+            return fail(c, RWKV7_ENOMEM, "the caller's device allocator refused %zu bytes", bytes);
+        if ((uintptr_t)q & 255u) {
+            c->alloc.release(c->alloc.user, q);
+            return fail(c, RWKV7_EINVAL, "the caller's device allocator returned a pointer not 256-byte aligned");
+        }
+    } else {
+        cudaError_t e = cudaMalloc(&q, bytes);
+        if (e != cudaSuccess)
+            return fail(c, RWKV7_ENOMEM, "cudaMalloc(%zu bytes): %s", count * sizeof(T), cudaGetErrorString(e));
+    }
     c->allocs.push_back(q);
-    e = cudaMemset(q, 0, count * sizeof(T) + 256);
+    cudaError_t e = cudaMemset(q, 0, bytes);
     if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "cudaMemset: %s", cudaGetErrorString(e));
     *p = (T *)q;
     return RWKV7_OK;
@@ -312,9 +339,10 @@ struct Seg {
 };
 
 int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *nz_out, const uint32_t *nz_skip,
-             const LaunchCfg &lc, int mode) {
+             const LaunchCfg &lc, int mode, unsigned long long *tl = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof p);
+    p.tl = tl;
     p.nz_count = nz_out ? c->nzstat : nullptr;
     int nmaps = 0;
     int wslot[W_COUNT], aslot[A_COUNT];
@@ -432,12 +460,21 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
 
 const __half *LW(rwkv7_ctx *c, int kind, int l) { return c->w[kind] + (size_t)l * layer_elems(c, kind); }
 
+constexpr int TL_MAX_LAUNCHES = 4096;
+
 // Enqueue one fused step for rows [0, B) of the activation buffers (slots and
-// tokens already in c->slots / c->tokens).
-int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, int mode, Prof *pf = nullptr) {
+// tokens already in c->slots / c->tokens).  With `tcls`, every launch gets its
+// four timeline words in c->tlbuf (in launch order) and its class is appended.
+int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, int mode, Prof *pf = nullptr,
+                 std::vector<int> *tcls = nullptr) {
     LaunchCfg lc{st, mode != 2 && pf == nullptr};
     LaunchCfg lc0{st, false};
     cudaError_t e = cudaSuccess;
+    auto tlp = [&](int cls) -> unsigned long long * {
+        if (!tcls || (int)tcls->size() >= TL_MAX_LAUNCHES) return nullptr;
+        tcls->push_back(cls);
+        return c->tlbuf + 4 * (tcls->size() - 1);
+    };
     // optional CUDA-event bracketing of every launch (profiling mode only)
     auto pb = [&](int cls) {
         if (!pf) return;
@@ -473,7 +510,9 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     ep.ln_w = c->w[W_LN0W];
     ep.ln_b = c->w[W_LN0B];
     pb(P_EMBED);
+    ep.tl = tlp(P_EMBED);
     launch_embed(ep, lc0, &e);
+    ep.tl = nullptr;
     pe();
     if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "embed launch: %s", cudaGetErrorString(e));
     int rc;
@@ -497,6 +536,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         m.nsplit = px_splits;
         m.split_stride = xstride;
         pb(P_LN_MIX);
+        m.tl = tlp(P_LN_MIX);
         launch_ln_mix(m, 6, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
@@ -521,7 +561,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
             g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, s1};
         }
         pb(P_GEMM_PROJ);
-        if ((rc = run_gemm(c, l, g1, n1, B, nullptr, nullptr, lc, mode))) return rc;
+        if ((rc = run_gemm(c, l, g1, n1, B, nullptr, nullptr, lc, mode, tlp(P_GEMM_PROJ)))) return rc;
         pe();
         // LoRA down: add the slabs, activation, fp16 (the LoRA-up GEMM's operands)
         if (!fin_fused) {
@@ -535,6 +575,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         lf.act[0] = 1; lf.act[1] = 0; lf.act[2] = 0; lf.act[3] = 2;
         lf.bcap = c->bcap;
         pb(P_LORA_FIN);
+        lf.tl = tlp(P_LORA_FIN);
         launch_lora_fin(lf, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "lora_fin launch: %s", cudaGetErrorString(e));
@@ -547,7 +588,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         if (l > 0) g2[n2++] = {L_V2, A_HV, c->hv, c->rv, EPI_SIGMOID_BIAS, c->vg, d, LW(c, L_V0, l), 1};
         g2[n2++] = {L_G2, A_HG, c->hg, c->rg, EPI_F32, c->g, d, nullptr, 1};
         pb(P_GEMM_LORA);
-        if ((rc = run_gemm(c, l, g2, n2, B, nullptr, nullptr, lc, mode))) return rc;
+        if ((rc = run_gemm(c, l, g2, n2, B, nullptr, nullptr, lc, mode, tlp(P_GEMM_LORA)))) return rc;
         pe();
         // WKV7 + GroupNorm + bonus + gate (adds the r, k, v slabs)
         WkvParams wp;
@@ -577,13 +618,14 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         wp.z = c->z;
         wp.err = c->errw;
         pb(P_WKV);
+        wp.tl = tlp(P_WKV);
         launch_wkv(wp, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "wkv launch: %s", cudaGetErrorString(e));
         // G3: output projection, as residual partial slabs
         Seg g3[1] = {{L_WO, A_Z, c->z, d, EPI_F32, c->px, d, nullptr, s3}};
         pb(P_GEMM_OUT);
-        if ((rc = run_gemm(c, l, g3, 1, B, nullptr, nullptr, lc, mode))) return rc;
+        if ((rc = run_gemm(c, l, g3, 1, B, nullptr, nullptr, lc, mode, tlp(P_GEMM_OUT)))) return rc;
         pe();
         px_splits = s3;
         // (x += slabs) + LN2 + token shift + mix
@@ -598,18 +640,19 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         m2.nsplit = px_splits;
         m2.split_stride = xstride;
         pb(P_LN_MIX);
+        m2.tl = tlp(P_LN_MIX);
         launch_ln_mix(m2, 1, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
         // G4: key + ReLU^2 (+ nonzero flags per 64 hidden units)
         Seg g4[1] = {{L_FK, A_XKF, c->xk, d, EPI_RELU2, c->h, c->F, nullptr, 1}};
         pb(P_GEMM_KEY);
-        if ((rc = run_gemm(c, l, g4, 1, B, c->nz, nullptr, lc, mode))) return rc;
+        if ((rc = run_gemm(c, l, g4, 1, B, c->nz, nullptr, lc, mode, tlp(P_GEMM_KEY)))) return rc;
         pe();
         // G5: value over the nonzero hidden blocks, as residual partial slabs
         Seg g5[1] = {{L_FV, A_H, c->h, c->F, EPI_F32, c->px, d, nullptr, s5}};
         pb(P_GEMM_VALUE);
-        if ((rc = run_gemm(c, l, g5, 1, B, nullptr, c->nz, lc, mode))) return rc;
+        if ((rc = run_gemm(c, l, g5, 1, B, nullptr, c->nz, lc, mode, tlp(P_GEMM_VALUE)))) return rc;
         pe();
         px_splits = s5;
     }
@@ -622,12 +665,13 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         o.nsplit = px_splits;
         o.split_stride = xstride;
         pb(P_LN_OUT);
+        o.tl = tlp(P_LN_OUT);
         launch_ln_out(o, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_out launch: %s", cudaGetErrorString(e));
         Seg gh[1] = {{W_HEAD, A_XO, c->xo, d, EPI_F32, c->logits, c->V, nullptr, 1}};
         pb(P_GEMM_HEAD);
-        if ((rc = run_gemm(c, 0, gh, 1, B, nullptr, nullptr, lc, mode))) return rc;
+        if ((rc = run_gemm(c, 0, gh, 1, B, nullptr, nullptr, lc, mode, tlp(P_GEMM_HEAD)))) return rc;
         pe();
         if (sample) {
             SamplerParams sp;
@@ -644,6 +688,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
             sp.next = c->next;
             sp.err = c->errw;
             pb(P_SAMPLER);
+            sp.tl = tlp(P_SAMPLER);
             launch_sampler(sp, lc, &e);
             pe();
             if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "sampler launch: %s", cudaGetErrorString(e));
@@ -1024,17 +1069,17 @@ int enqueue_prefill(rwkv7_ctx *c, cudaStream_t st, int slot, int n, bool head) {
     return RWKV7_OK;
 }
 
-int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
-    if (c->mode == 3) return run_persistent(c, B, head, sample);
-    c->nz_considered += (unsigned long long)c->L * ((c->F + 63) / 64);
-    if (c->mode != 0) return enqueue_step(c, c->stream, B, head, sample, c->mode);
-    auto key = std::make_tuple(B, (int)head, (int)sample, c->mode);
+// The CUDA graph of one fused step (captured on first use per key).  A timeline
+// graph is the same step with every launch stamping its words in c->tlbuf.
+int step_graph(rwkv7_ctx *c, int B, bool head, bool sample, bool timeline, cudaGraphExec_t *out) {
+    auto key = std::make_tuple(B, (int)head, (int)sample, c->mode, (int)timeline);
     auto it = c->graphs.find(key);
     if (it == c->graphs.end()) {
         cudaGraph_t g = nullptr;
+        std::vector<int> cls;
         if (!c->cap_stream) CK(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
         CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
-        int rc = enqueue_step(c, c->cap_stream, B, head, sample, 0);
+        int rc = enqueue_step(c, c->cap_stream, B, head, sample, 0, nullptr, timeline ? &cls : nullptr);
         cudaError_t e2 = cudaStreamEndCapture(c->cap_stream, &g);
         if (rc) {
             if (g) cudaGraphDestroy(g);
@@ -1046,8 +1091,20 @@ int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
         cudaGraphDestroy(g);
         if (e3 != cudaSuccess) return fail(c, RWKV7_ECUDA, "graph instantiate: %s", cudaGetErrorString(e3));
         it = c->graphs.emplace(key, ex).first;
+        if (timeline) c->tl_classes[std::make_tuple(B, (int)head, (int)sample)] = cls;
     }
-    CK(cudaGraphLaunch(it->second, c->stream));
+    *out = it->second;
+    return RWKV7_OK;
+}
+
+int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
+    if (c->mode == 3) return run_persistent(c, B, head, sample);
+    c->nz_considered += (unsigned long long)c->L * ((c->F + 63) / 64);
+    if (c->mode != 0) return enqueue_step(c, c->stream, B, head, sample, c->mode);
+    cudaGraphExec_t ex = nullptr;
+    int rc = step_graph(c, B, head, sample, false, &ex);
+    if (rc) return rc;
+    CK(cudaGraphLaunch(ex, c->stream));
     return RWKV7_OK;
 }
 
@@ -1104,6 +1161,10 @@ int rwkv7_create_ex(const rwkv7_config *cfg, int32_t weight_bits, void *cuda_str
         if (r < 8 || r % 8) return RWKV7_EINVAL;
     if (g.vocab % 8) return RWKV7_EINVAL;
     rwkv7_ctx *c = new rwkv7_ctx();
+    {
+        std::lock_guard<std::mutex> lk(g_alloc_mu);
+        c->alloc = g_alloc;
+    }
     c->cfg = g;
     c->wbits = weight_bits;
     c->L = g.n_layer;
@@ -1235,8 +1296,35 @@ void rwkv7_destroy(rwkv7_ctx *c) {
     for (auto &kv : c->graphs) cudaGraphExecDestroy(kv.second);
     for (cudaEvent_t ev : c->prof.ev) cudaEventDestroy(ev);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
-    for (void *p : c->allocs) cudaFree(p);
+    for (void *p : c->allocs) {
+        if (c->alloc.release)
+            c->alloc.release(c->alloc.user, p);
+        else
+            cudaFree(p);
+    }
     delete c;
+}
+
+int rwkv7_set_device_allocator(rwkv7_alloc_fn alloc, rwkv7_free_fn release, void *user) {
+    if ((alloc == nullptr) != (release == nullptr)) return RWKV7_EINVAL;
+    std::lock_guard<std::mutex> lk(g_alloc_mu);
+    g_alloc.alloc = alloc;
+    g_alloc.release = release;
+    g_alloc.user = user;
+    return RWKV7_OK;
+}
+
+int rwkv7_debug_latch_error(rwkv7_ctx *c, uint32_t flags) {
+    if (!c) return RWKV7_EINVAL;
+    if (!c->errw) return fail(c, RWKV7_ESTATE, "context not created");
+    // stream-ordered read-modify-write of the error word on the host side of a
+    // synchronisation: the word is OR-ed exactly as a kernel would latch it
+    CK(cudaStreamSynchronize(c->stream));
+    uint32_t w = 0;
+    CK(cudaMemcpy(&w, c->errw, 4, cudaMemcpyDeviceToHost));
+    w |= flags;
+    CK(cudaMemcpy(c->errw, &w, 4, cudaMemcpyHostToDevice));
+    return RWKV7_OK;
 }
 
 const char *rwkv7_last_error(const rwkv7_ctx *c) { return c ? c->err.c_str() : "null context"; }
@@ -1634,6 +1722,41 @@ int rwkv7_profile_step(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_to
         ms_out[pf.cls[i]] += ms;
         launches_out[pf.cls[i]] += 1;
     }
+    return RWKV7_OK;
+}
+
+int rwkv7_step_timeline(rwkv7_ctx *c, const int32_t *d_slots, const int32_t *d_tokens, int32_t B,
+                        int32_t with_sampling, uint64_t *host_times, int32_t *host_classes, int32_t max_launches,
+                        int32_t *n_launches) {
+    if (!c) return RWKV7_EINVAL;
+    if (!d_slots || !d_tokens || !host_times || !host_classes || !n_launches || B < 1 || B > c->bcap ||
+        max_launches < 1)
+        return fail(c, RWKV7_EINVAL, "bad timeline arguments (B must be <= %d)", c->bcap);
+    if (c->mode != 0 && c->mode != 1) return fail(c, RWKV7_EINVAL, "the timeline covers modes 0 and 1");
+    int rc;
+    if ((rc = check_ready(c))) return rc;
+    if (!c->tlbuf && (rc = dalloc(c, &c->tlbuf, (size_t)4 * TL_MAX_LAUNCHES))) return rc;
+    if (d_slots != c->slots) CK(cudaMemcpyAsync(c->slots, d_slots, (size_t)B * 4, cudaMemcpyDeviceToDevice, c->stream));
+    if (d_tokens != c->tokens)
+        CK(cudaMemcpyAsync(c->tokens, d_tokens, (size_t)B * 4, cudaMemcpyDeviceToDevice, c->stream));
+    // start words to all ones, release-max and end words to zero
+    CK(cudaMemsetAsync(c->tlbuf, 0xFF, (size_t)32 * TL_MAX_LAUNCHES, c->stream));
+    CK(cudaMemset2DAsync(c->tlbuf + 2, 32, 0, 16, TL_MAX_LAUNCHES, c->stream));
+    c->nz_considered += (unsigned long long)c->L * ((c->F + 63) / 64);
+    std::vector<int> cls;
+    if (c->mode == 0) {
+        cudaGraphExec_t ex = nullptr;
+        if ((rc = step_graph(c, B, true, with_sampling != 0, true, &ex))) return rc;
+        cls = c->tl_classes[std::make_tuple(B, 1, (int)(with_sampling != 0))];
+        CK(cudaGraphLaunch(ex, c->stream));
+    } else {
+        if ((rc = enqueue_step(c, c->stream, B, true, with_sampling != 0, c->mode, nullptr, &cls))) return rc;
+    }
+    CK(cudaStreamSynchronize(c->stream));
+    const int n = std::min((int)cls.size(), (int)max_launches);
+    CK(cudaMemcpy(host_times, c->tlbuf, (size_t)n * 32, cudaMemcpyDeviceToHost));
+    for (int i = 0; i < n; ++i) host_classes[i] = cls[i];
+    *n_launches = n;
     return RWKV7_OK;
 }
 

@@ -204,8 +204,10 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SmpShared &sm = *reinterpret_cast<SmpShared *>(smem_raw);
     const int b = blockIdx.x, tid = threadIdx.x;
+    if (tid == 0) tl_start(p.tl);
     pdl_wait();
     pdl_launch();
+    if (tid == 0) tl_release(p.tl);
     const int slot = p.slots[b];
     if (slot < 0 || slot >= p.n_slots) {
         if (tid == 0) {
@@ -260,6 +262,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
                     bj = sm.wi[w];
                 }
             p.next[b] = (bj < V) ? bj : 0;
+            tl_end(p.tl);
         }
         return;
     }
@@ -513,6 +516,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
         p.next[b] = tok >= 0 ? tok : 0;
         if (tok < 0) atomicOr(p.err, ERR_CONFIG);
         p.ndraw[slot] = nd + 1ull;
+        tl_end(p.tl);
     }
 }
 
