@@ -74,6 +74,8 @@ def class_bytes(dm: synth.Dims, B: int):
         "gemm_out": L * (d * d * f16 + B * d * f16 + 2 * B * d * f32),
         "gemm_key": L * (F * d * f16 + B * d * f16 + B * F * f16),
         "gemm_value": L * (d * F * f16 + B * F * f16 + 2 * B * d * f32),
+        # the key and value projections as one launch (fused channel mix)
+        "gemm_ffn": L * (F * d * f16 + B * d * f16 + B * F * f16) + L * (d * F * f16 + B * F * f16 + 2 * B * d * f32),
         "ln_out": B * d * (f32 + f16),
         "gemm_head": V * d * f16 + B * d * f16 + B * V * f32,
         "sampler": B * V * f32,
@@ -145,11 +147,30 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_baseline(weights, dm, wl, seconds=15.0):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(weights, dm, wl, seconds=15.0, threads=None):
     """The oracle, as it stands, on a bounded sample of the workload: decode
     tokens of one slot (after a short prompt) until ~`seconds` have passed."""
     import oracle
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     oracle.set_threads(threads)
     m = oracle.Model(weights, dm)
     st = m.new_state()
@@ -164,7 +185,7 @@ def cpu_baseline(weights, dm, wl, seconds=15.0):
         if time.perf_counter() - t0 >= seconds or n >= 2000:
             break
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "tok/s", "cores": threads, "kind": "oracle",
+    return {"value": n / dt, "unit": "tok/s", "cores": threads, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{n} greedy decode tokens of 1 slot of the {dm.name} shape (fp64 oracle, OpenMP over "
                       f"matrix rows, {threads} threads), {dt:.1f} s"}
 
@@ -209,10 +230,12 @@ def _config(wl, dm, args):
             "l2": "inputs larger than L2 (weights + states per step >> 126 MB), no flush"}
 
 
-def run_trace_bench(args, wl):
+def run_trace_bench(args, wl, ctx=None, name=None):
     """The continuous-batching trace: every request to completion through the
     worker loop (recurrent_decode_gb300.trace); value = generated tokens per
-    second of wall time, prefills included."""
+    second of wall time, prefills included.  With ctx (a context of the trace's
+    shape with enough slots) the trace runs on it and the line is returned
+    instead of printed."""
     import torch
     import recurrent_decode_gb300 as rd
     from recurrent_decode_gb300.trace import Request, run_trace
@@ -222,13 +245,15 @@ def run_trace_bench(args, wl):
     torch.cuda.set_device(local)
     from recurrent_decode_gb300.prefix_cache import PrefixStateCache
     dm = synth.Dims(wl["shape"])
-    weights = synth.make_weights(wl["shape"])
     n_cache = wl.get("cache_slots", 0)
-    ctx = rd.Rwkv7(dm, wl["n_slots"] + n_cache)
-    ctx.set_weights(weights)
-    del weights
-    if args.mode >= 0:
-        ctx.set_mode(args.mode)
+    own = ctx is None
+    if own:
+        weights = synth.make_weights(wl["shape"])
+        ctx = rd.Rwkv7(dm, wl["n_slots"] + n_cache)
+        ctx.set_weights(weights)
+        del weights
+        if args.mode >= 0:
+            ctx.set_mode(args.mode)
     lens = synth.trace_requests(wl["n_req"], *wl["prompt_range"], *wl["out_range"])
     prefix = (synth.prompt_tokens(dm.vocab, 1, wl["shared_prefix"], seed=9999)[0]
               if wl.get("shared_prefix") else np.zeros(0, np.int32))
@@ -264,14 +289,15 @@ def run_trace_bench(args, wl):
         uncached, _ = one_run(None)
     cache = PrefixStateCache(ctx, range(wl["n_slots"], wl["n_slots"] + n_cache)) if n_cache else None
     stats, clocks = one_run(cache)
-    ctx.close()
+    if own:
+        ctx.close()
     ttft = np.array(stats.ttft_s)
     total_in = stats.prefill_tokens + stats.decode_fed_tokens + stats.generated
     line = {"metric": METRIC, "value": world * stats.generated / stats.wall_s, "unit": "tok/s", "n_gpus": world,
             "steps": stats.rounds, "warmup": 0, "ms_per_step": stats.wall_s * 1e3 / max(1, stats.rounds),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic",
-            "config": {"workload": f"continuous-batching trace on the {dm.name} shape ({args.config})",
+            "config": {"workload": f"continuous-batching trace on the {dm.name} shape ({name or args.config})",
                        "shape": dm.name, "slots": wl["n_slots"], "requests": wl["n_req"],
                        "prompt_range": list(wl["prompt_range"]), "output_range": list(wl["out_range"]),
                        "decode_prefill_ratio": wl["decode_prefill_ratio"],
@@ -292,9 +318,121 @@ def run_trace_bench(args, wl):
                          "prefill_tokens": uncached.prefill_tokens,
                          "ttft_s_p50": float(np.percentile(ut, 50)), "ttft_s_p90": float(np.percentile(ut, 90))},
             "note": "value / trace: the run with the cache; the same requests without it under 'uncached'"}
+    if not own:
+        return line
     if rank == 0:
         print(json.dumps(line))
     return 0
+
+
+def in_graph_times(ctx, slots, tokens, with_sampling=True, reps=3):
+    """Per-class time each kernel class adds to the graph-replayed step, from the
+    in-graph timeline (rwkv7_step_timeline): launch k adds end_k - end_{k-1}.
+    Returns ({class: (ms per step, launches)}, timeline step ms); the median of
+    `reps` timeline steps per class."""
+    runs = []
+    for _ in range(reps):
+        t, cls = ctx.step_timeline(slots, tokens, with_sampling=with_sampling)
+        add = {}
+        for k in range(len(cls)):
+            prev = t[k - 1, 3] if k else t[0, 0]
+            a = add.setdefault(cls[k], [0.0, 0])
+            a[0] += (t[k, 3] - prev) / 1e6
+            a[1] += 1
+        runs.append((add, (t[-1, 3] - t[0, 0]) / 1e6))
+    out = {}
+    for c in runs[0][0]:
+        out[c] = (statistics.median(r[0][c][0] for r in runs), runs[0][0][c][1])
+    return out, statistics.median(r[1] for r in runs)
+
+
+def union_sweep(dev, fractions=(1.0, 0.75, 0.5, 0.25, 0.1), n_layer=8, B=64, steps=16):
+    """The sparse channel-mix value projection on weights whose key rows are
+    zero for a chosen share of the 64-row hidden blocks (every layer, seeded):
+    those hidden blocks are zero for every slot, so the value projection skips
+    their 64 rows of the value matrix.  Reports, per union fraction, the value
+    projection's in-graph time per launch, the whole step, and the roofline
+    counting only the union's value rows."""
+    import torch
+    import recurrent_decode_gb300 as rd
+    dm = synth.Dims("2.9b", n_layer)
+    W = synth.make_weights("2.9b", n_layer=n_layer)
+    ctx = rd.Rwkv7(dm, B)
+    ctx.set_weights(W)
+    for s in range(B):
+        ctx.set_sampling(s, greedy=True)
+    slots = torch.arange(B, dtype=torch.int32, device=dev)
+    tokens = torch.from_numpy(synth.prompt_tokens(dm.vocab, B, 1)[:, 0].copy()).to(dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    nblk = dm.d_ffn // 64
+    rng = np.random.default_rng(5)
+    peak, peak_kind = _peaks()
+    rows = []
+    for f in fractions:
+        keep = np.zeros(nblk, bool)
+        keep[rng.permutation(nblk)[:max(1, round(f * nblk))]] = True
+        for l in range(n_layer):
+            k = W[f"blocks.{l}.ffn.key"].copy()
+            k.reshape(nblk, 64, dm.d_model)[~keep] = 0
+            ctx.set_weight(f"blocks.{l}.ffn.key", k)
+        for _ in range(3):
+            ctx.decode_step(slots, tokens, None, nxt)
+        ctx.synchronize()
+        ctx.ffn_union_stats()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            ctx.decode_step(slots, tokens, None, nxt)
+        e1.record()
+        torch.cuda.synchronize()
+        nz, tot = ctx.ffn_union_stats()
+        ig, _ = in_graph_times(ctx, slots, tokens, with_sampling=False)
+        v_ms, v_n = ig["gemm_value"]
+        union = nz / max(1, tot)
+        vbytes = union * dm.d_model * dm.d_ffn * 2  # value rows of the union, per launch
+        rows.append({"union_fraction": union, "value_us_per_launch": 1e3 * v_ms / v_n,
+                     "step_ms": e0.elapsed_time(e1) / steps,
+                     "union_roofline_GBps": vbytes / (v_ms / v_n / 1e3) / 1e9,
+                     "union_roofline_frac": vbytes / (v_ms / v_n / 1e3) / 1e9 / peak})
+    ctx.close()
+    return {"shape": f"2.9b, {n_layer} layers, B={B}", "peak_kind": peak_kind, "points": rows,
+            "note": "ffn.key rows zeroed for (1 - fraction) of the 64-row hidden blocks; value projection time is "
+                    "its in-graph time per launch (rwkv7_step_timeline); the roofline counts union rows only"}
+
+
+def shrink_sweep(ctx, dm, dev, batches=(256, 128, 64, 32, 16, 8, 4, 2, 1), steps=20):
+    """Batch shrink: the same context decoding B = 256 ... 1 slots.  Per B: the
+    first step at that B timed on the host (it captures and instantiates the
+    step's CUDA graph), then ms/step of the replayed graph and the whole-step
+    roofline."""
+    import torch
+    peak, peak_kind = _peaks()
+    rows = []
+    for B in batches:
+        slots = torch.arange(B, dtype=torch.int32, device=dev)
+        tokens = torch.from_numpy(synth.prompt_tokens(dm.vocab, B, 1, seed=3)[:, 0].copy()).to(dev)
+        nxt = torch.empty(B, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ctx.decode_step(slots, tokens, None, nxt)
+        torch.cuda.synchronize()
+        first_ms = (time.perf_counter() - t0) * 1e3
+        for _ in range(3):
+            ctx.decode_step(slots, tokens, None, nxt)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            ctx.decode_step(slots, tokens, None, nxt)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        gbs = step_bytes(dm, B) / (ms / 1e3) / 1e9
+        rows.append({"B": B, "first_step_ms": first_ms, "ms_per_step": ms, "tok_s": B / (ms / 1e3),
+                     "step_GBps": gbs, "frac_of_peak": gbs / peak, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS})
+    ctx.synchronize()
+    return {"shape": dm.name, "peak_kind": peak_kind, "points": rows,
+            "note": "greedy steps; first_step_ms includes capturing and instantiating the step graph for a B "
+                    "not seen before"}
 
 
 def secondary(config, steps, args, dev, world, int8=False):
@@ -377,7 +515,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="2.9b", choices=list(synth.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=64)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run a model with this many layers of the shape's sizes")
@@ -385,7 +523,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the 7.2B-shape measurement added to the 2.9B line")
     ap.add_argument("--mode", type=int, default=-1,
-                    help="implementation: 0 multi-kernel CUDA graph, 3 persistent kernel (default: library default)")
+                    help="implementation: 0 CUDA-graph replay, 1 direct launches, 2 CUDA-core cross-check "
+                         "(default: library default)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = dict(synth.WORKLOADS[args.config])
@@ -410,7 +549,10 @@ def main():
 
     B = wl["B"]
     weights = synth.make_weights(wl["shape"], n_layer=args.layers or None)
-    ctx = rd.Rwkv7(dm, B)
+    full = args.config == "2.9b" and world == 1 and not args.layers and not args.prompt and not args.no_secondary
+    # the headline context keeps 256 slots so that the batch-shrink sweep and the
+    # trace can run on it after the timed steps (slots beyond B are untouched then)
+    ctx = rd.Rwkv7(dm, 256 if full else B)
     ctx.set_weights(weights)
     if args.mode >= 0:
         ctx.set_mode(args.mode)
@@ -497,21 +639,25 @@ def main():
                "note": "one slot, 4 chunks of 256 tokens; FLOPs = 2 x non-embedding, non-head parameters x tokens "
                        "+ the head for the last token"}
 
-    # per-kernel-class device time of one directly launched step (events)
+    # time each kernel class adds to the graph-replayed step (in-graph timeline),
+    # and the device time of each class in one directly launched step (events)
+    ig, tl_ms = in_graph_times(ctx, slots, tokens, with_sampling=True)
     prof = ctx.profile_step(slots, tokens, with_sampling=True)
     cb = class_bytes(dm, B)
     peak, peak_kind = _peaks()
-    gemm_cls = [k for k in prof if k.startswith("gemm") and k in cb]
-    gemm_ms = sum(prof[k][0] for k in gemm_cls)
-    gemm_n = sum(prof[k][1] for k in gemm_cls)
-    gemm_bytes = sum(cb[k] for k in gemm_cls)
-    kern = {
-        "gemm_tc_kernel": (gemm_ms, gemm_n, gemm_bytes),
-        "wkv_kernel": (prof["wkv"][0], prof["wkv"][1], cb["wkv"]),
-    }
+
+    def family(times):
+        gemm_cls = [k for k in times if k.startswith("gemm") and k in cb]
+        return {"gemm_tc_kernel": (sum(times[k][0] for k in gemm_cls), sum(times[k][1] for k in gemm_cls),
+                                   sum(cb[k] for k in gemm_cls)),
+                "wkv_kernel": (times["wkv"][0], times["wkv"][1], cb["wkv"])}
+
+    kern = family(ig)
     dom = max(kern, key=lambda k: kern[k][0])
     dms, dn, dbytes = kern[dom]
     achieved = (dbytes / dn) / ((dms / dn) / 1e3) / 1e9
+    iso_ms, iso_n, _ = family(prof)[dom]
+    iso_achieved = (dbytes / dn) / ((iso_ms / iso_n) / 1e3) / 1e9
     tr = NCU_TRAFFIC.get((dom, wl["shape"])) if not args.layers else None
     traffic = None
     if tr is not None:
@@ -526,9 +672,16 @@ def main():
         "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": _config(wl, dm, args),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": dbytes / dn, "launches_per_step": dn},
+                     "algorithmic_bytes_per_launch": dbytes / dn, "launches_per_step": dn,
+                     "kernel_ms_per_step": dms,
+                     "timing": "in-graph: the time this kernel's launches add to the replayed step "
+                               "(rwkv7_step_timeline, GPU global timer)",
+                     "isolated": {"achieved": iso_achieved, "frac": iso_achieved / peak, "ms_per_step": iso_ms,
+                                  "timing": "directly launched step, CUDA events around each launch"}},
         "step_roofline": {"bytes_per_step": sb, "achieved_GBps": step_gbs,
                           "frac_of_8TBps": step_gbs / NOMINAL_HBM_GBS, "frac_of_peak": step_gbs / peak},
+        "in_graph_ms_per_step": {k: round(v[0], 4) for k, v in ig.items()},
+        "timeline_step_ms": tl_ms,
         "kernel_ms_per_step": {k: round(v[0], 4) for k, v in prof.items()},
         "e2e": {"value": e2e_val, "unit": "tok/s", "h2d_bytes_per_step": 2 * B * 4, "d2h_bytes_per_step": B * 4,
                 "steps": args.e2e_steps},
@@ -539,14 +692,24 @@ def main():
                               "over the timed steps; the roofline counts the dense bytes"},
         "clocks": clocks,
     }
+    if full:
+        line["batch_shrink"] = shrink_sweep(ctx, dm, dev)
+        # the continuous-batching trace at the pages' measured prefill mix, on the same context
+        tr = run_trace_bench(args, synth.WORKLOADS["trace-3pct"], ctx=ctx, name="trace-3pct")
+        line["trace_3pct"] = {"value": tr["value"], "unit": tr["unit"], "config": tr["config"],
+                              "trace": tr["trace"], "clocks": tr["clocks"]}
     ctx.close()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(weights, dm, wl, args.cpu_seconds)
-    if args.config == "2.9b" and world == 1 and not args.layers and not args.prompt and not args.no_secondary:
+        cb_all = cpu_baseline(weights, dm, wl, args.cpu_seconds)
+        cb_one = cpu_baseline(weights, dm, wl, args.cpu_seconds / 2, threads=1)
+        cb_all["single_thread"] = {"value": cb_one["value"], "cores": 1, "sample": cb_one["sample"]}
+        line["cpu_baseline"] = cb_all
+    if full:
         # the metric names both shapes: the 7.2B workload rides along on the same line
         line["secondary"] = secondary("7.2b", max(16, min(64, args.steps)), args, dev, world)
         # the int8 weight variant of the headline workload (a separate row, not the headline)
         line["int8"] = secondary("2.9b", max(16, min(256, args.steps)), args, dev, world, int8=True)
+        line["ffn_union_sweep"] = union_sweep(dev)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

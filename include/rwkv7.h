@@ -231,6 +231,8 @@ RWKV7_API int rwkv7_sample_batch(rwkv7_ctx *ctx, const int32_t *d_slots, const f
  *  d_err       device uint32 word; flags are OR-ed into it (1 = row index out of
  *              range, 16 = no token could be kept); the caller clears it
  *  cuda_stream the cudaStream_t to launch on (NULL = legacy default stream)
+ *              -- it and every pointer above must belong to the CURRENT device
+ *              (the one whose scratch address the call uses)
  *  err_msg     if not NULL, receives a static text describing a host-side error
  *              ("" on success); valid until the next call from the same thread
  *
@@ -263,10 +265,8 @@ RWKV7_API int rwkv7_debug_latch_error(rwkv7_ctx *ctx, uint32_t flags);
 
 /* Select the decode implementation: 0 = tensor-core kernels with CUDA-graph
  * replay (default), 1 = the same kernels launched directly, 2 = CUDA-core
- * (SIMT) projection kernels launched directly (a slow cross-check), 3 = one
- * persistent cooperative kernel for the whole step (B <= 256; correct, and
- * slower than mode 0 today).  Modes 2 and 3 take fp16 weights only.
- * RWKV7_EINVAL for another value. */
+ * (SIMT) projection kernels launched directly (a slow cross-check; fp16
+ * weights only).  RWKV7_EINVAL for another value. */
 RWKV7_API int rwkv7_set_mode(rwkv7_ctx *ctx, int32_t mode);
 
 /* The ctx's own device I/O buffers for a fused step (capacity min(n_slots, 256)
@@ -280,8 +280,7 @@ RWKV7_API int rwkv7_get_io_buffers(rwkv7_ctx *ctx, int32_t **d_slots, int32_t **
  * value matrix whose hidden block is nonzero for some slot of the step.  This
  * returns, since the previous call (or rwkv7_create), the number of such
  * nonzero blocks and the number of blocks considered (layers x d_ffn/64 per
- * step or prefill chunk; the persistent mode computes the value projection
- * densely and is not counted), then resets both.  Synchronous. */
+ * step or prefill chunk), then resets both.  Synchronous. */
 RWKV7_API int rwkv7_ffn_union_stats(rwkv7_ctx *ctx, uint64_t *nonzero_blocks, uint64_t *blocks);
 
 /* Kernel classes of rwkv7_profile_step, in output order. */
@@ -297,7 +296,8 @@ RWKV7_API int rwkv7_ffn_union_stats(rwkv7_ctx *ctx, uint64_t *nonzero_blocks, ui
 #define RWKV7_PROF_GEMM_HEAD 9   /* head projection to fp32 logits */
 #define RWKV7_PROF_SAMPLER 10    /* penalties + sampling */
 #define RWKV7_PROF_LORA_FIN 11   /* LoRA-down split sums + tanh / sigmoid to fp16 hidden */
-#define RWKV7_PROF_CLASSES 12
+#define RWKV7_PROF_GEMM_FFN 12   /* channel-mix key + ReLU^2 and value + residual in one launch */
+#define RWKV7_PROF_CLASSES 13
 
 /* Run one step of B <= min(n_slots, 256) slots with every kernel launched
  * directly (no graph, no dependent-launch overlap) and bracketed by CUDA events
@@ -318,7 +318,7 @@ RWKV7_API int rwkv7_profile_step(rwkv7_ctx *ctx, const int32_t *d_slots, const i
  * RWKV7_PROF_* class; *n_launches the number of launches (at most
  * max_launches).  The end of launch i minus the end of launch i - 1 is the time
  * that launch adds to the step.  The step is a real step: the slots' states
- * advance.  Synchronous; RWKV7_EINVAL for bad arguments or mode 2 / 3. */
+ * advance.  Synchronous; RWKV7_EINVAL for bad arguments or mode 2. */
 RWKV7_API int rwkv7_step_timeline(rwkv7_ctx *ctx, const int32_t *d_slots, const int32_t *d_tokens, int32_t B,
                                   int32_t with_sampling, uint64_t *host_times, int32_t *host_classes,
                                   int32_t max_launches, int32_t *n_launches);

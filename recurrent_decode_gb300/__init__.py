@@ -83,7 +83,7 @@ SIGNATURES = {
 SAMPLE_STATIC_MAX_ELEMS = 1 << 22
 
 PROF_CLASSES = ["embed", "ln_mix", "gemm_proj", "gemm_lora", "wkv", "gemm_out", "gemm_key", "gemm_value",
-                "ln_out", "gemm_head", "sampler", "lora_fin"]
+                "ln_out", "gemm_head", "sampler", "lora_fin", "gemm_ffn"]
 
 _lib = None
 
@@ -136,7 +136,9 @@ def sample_rows_static(logits, rows, occ, params, ndraw, next_out, err, stream=N
     [n_rows] int64 (the uint64 draw counters), writing next_out [B] int32 and
     OR-ing error flags into err [1] int32.  The library allocates nothing for
     this call; its scratch is a fixed 16 MiB device array, so B * V must not
-    exceed SAMPLE_STATIC_MAX_ELEMS.  stream: torch.cuda.Stream or None (current)."""
+    exceed SAMPLE_STATIC_MAX_ELEMS.  Every buffer must be on one device; the
+    call runs with that device current.  stream: a torch.cuda.Stream of that
+    device, or None (its current stream)."""
     import torch
     lib = load_library()
     B, V = int(logits.shape[0]), int(logits.shape[1])
@@ -146,12 +148,21 @@ def sample_rows_static(logits, rows, occ, params, ndraw, next_out, err, stream=N
     if logits.dim() != 2 or occ.dim() != 2 or occ.shape[1] != V or rows.numel() != B \
             or next_out.numel() != B or ndraw.numel() != n_rows or err.numel() != 1:
         raise ValueError("shapes: logits [B][V], rows [B], occ [n_rows][V], ndraw [n_rows], next_out [B], err [1]")
-    st = stream if stream is not None else torch.cuda.current_stream()
+    dev = logits.device
+    for name, t in (("rows", rows), ("occ", occ), ("params", params), ("ndraw", ndraw), ("next_out", next_out),
+                    ("err", err)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, logits on {dev}: every buffer must be on one device")
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"the stream belongs to {stream.device}, the buffers to {dev}")
     msg = C.c_char_p()
-    rc = lib.rwkv7_sample_rows_static(_ptr(logits, torch.float32, "logits"), _ptr(rows, torch.int32, "rows"), B, V,
-                                      n_rows, _ptr(occ, torch.float32, "occ"), _ptr(params, torch.uint8, "params"),
-                                      _ptr(ndraw, torch.int64, "ndraw"), _ptr(next_out, torch.int32, "next_out"),
-                                      _ptr(err, torch.int32, "err"), C.c_void_p(st.cuda_stream), C.byref(msg))
+    with torch.cuda.device(dev):  # the library resolves its scratch and launches on the current device
+        st = stream if stream is not None else torch.cuda.current_stream(dev)
+        rc = lib.rwkv7_sample_rows_static(_ptr(logits, torch.float32, "logits"), _ptr(rows, torch.int32, "rows"),
+                                          B, V, n_rows, _ptr(occ, torch.float32, "occ"),
+                                          _ptr(params, torch.uint8, "params"), _ptr(ndraw, torch.int64, "ndraw"),
+                                          _ptr(next_out, torch.int32, "next_out"), _ptr(err, torch.int32, "err"),
+                                          C.c_void_p(st.cuda_stream), C.byref(msg))
     if rc != OK:
         raise RWKV7Error(rc, (msg.value or b"").decode())
 

@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "librwkv7.so")
-SOURCES = ["rwkv7_api.cu", "gemm.cu", "gemm8.cu", "elem.cu", "sampler.cu", "persist.cu"]
+SOURCES = ["rwkv7_api.cu", "gemm.cu", "gemm8.cu", "elem.cu", "sampler.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I" + os.path.join(os.path.dirname(HERE), "include")]

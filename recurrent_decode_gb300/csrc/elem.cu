@@ -713,11 +713,7 @@ void launch_wkv_prefill(const WkvSeqParams &p, const LaunchCfg &lc, cudaError_t 
     cudaLaunchConfig_t c1 = mkcfg(dim3(p.H, p.n), dim3(64), 0, lc, at);
     cudaError_t r = cudaLaunchKernelEx(&c1, wkv_vec_kernel, p);
     if (r == cudaSuccess) {
-        static bool attr_set = false;
-        if (!attr_set) {
-            r = cudaFuncSetAttribute(wkv_seq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(WsqSmem));
-            attr_set = r == cudaSuccess;
-        }
+        r = ensure_smem_attr((const void *)wkv_seq_kernel, (int)sizeof(WsqSmem));
     }
     if (r == cudaSuccess) {
         cudaLaunchConfig_t c2 = mkcfg(dim3(p.H, 4), dim3(128), sizeof(WsqSmem), lc, at);
@@ -738,15 +734,13 @@ void launch_ln_out(const ElemParams &p, const LaunchCfg &lc, cudaError_t *e) {
 }
 
 void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e) {
-    static bool attr_set = false;
     const size_t smem = sizeof(WkvSmem);
-    if (!attr_set) {
-        cudaError_t r = cudaFuncSetAttribute(wkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        cudaError_t r = ensure_smem_attr((const void *)wkv_kernel, (int)smem);
         if (r != cudaSuccess) {
             *e = r;
             return;
         }
-        attr_set = true;
     }
     cudaLaunchAttribute at[1];
     cudaLaunchConfig_t cfg = mkcfg(dim3(p.H, p.B), dim3(WKV_THREADS), smem, lc, at);

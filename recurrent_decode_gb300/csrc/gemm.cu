@@ -24,6 +24,50 @@
 #include "gemm_common.cuh"
 
 namespace rk {
+
+// The items of CTA c: its phase-0 items (two-phase launches: items [0, n0)
+// spread over CTAs [0, g0)), then its phase-1 items (items [n0, nitems) spread
+// over every CTA).  A single-phase launch has n0 = 0.
+struct ItemSpan {
+    int a0, a1, b0, b1;
+    __device__ __forceinline__ void init(const GemmParams &p, int c, int G) {
+        const int n0 = p.n0, n1 = p.nitems - p.n0;
+        a0 = a1 = 0;
+        if (c < p.g0) {
+            a0 = item_first(c, p.g0, n0);
+            a1 = item_first(c + 1, p.g0, n0);
+        }
+        b0 = n0 + item_first(c, G, n1);
+        b1 = n0 + item_first(c + 1, G, n1);
+    }
+    __device__ __forceinline__ int count() const { return (a1 - a0) + (b1 - b0); }
+    __device__ __forceinline__ int at(int k) const { return k < a1 - a0 ? a0 + k : b0 + (k - (a1 - a0)); }
+};
+
+// Bounded wait until *ctr >= target (acquire), giving up after WAIT_LIMIT_NS or
+// once *abort is set.
+__device__ __forceinline__ bool wait_count(const uint32_t *ctr, uint32_t target, volatile uint32_t *abort) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    const uint64_t t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(100);
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((it & 15u) == 0) {
+            if (*abort) return false;
+            if (gtimer() - t0 > WAIT_LIMIT_NS) return false;
+        }
+    }
+}
+__device__ __forceinline__ bool check_count(const uint32_t *ctr, uint32_t target) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    return v >= target;
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     // Segment descriptors and sparsity flags are staged in shared memory and the
@@ -34,7 +78,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
     __shared__ uint64_t flags_ready;
     __shared__ uint32_t s_ok;
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int S = p.stages, B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, nitems = p.nitems;
+    const int S = p.stages, B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, n0 = p.n0;
     const bool has_skip = p.nz_skip != nullptr;
     const uint32_t *skip = has_skip ? snz : nullptr;
     const uint32_t XKB = (uint32_t)npad * 128u;  // one activation k-block
@@ -51,7 +95,9 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const int i_begin = item_first(c, G, nitems), i_end = item_first(c + 1, G, nitems);
+    ItemSpan span;
+    span.init(p, c, G);
+    const int nmine = span.count();
     if (threadIdx.x == 0) tl_start(p.tl);
     uint32_t ncols = 32;
     while ((int)ncols < NB * npad) ncols <<= 1;
@@ -75,20 +121,32 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
 
     // Weight prefetch before the dependency wait (weights are constant), issued
     // before the TMEM allocation so it proceeds even while a predecessor's CTA
-    // still holds tensor memory on this SM.
-    int npre = 0;
+    // still holds tensor memory on this SM: the first npre stages of this CTA in
+    // walk order.  The sparsity flags of a skipping launch are known only later
+    // (after the dependency wait, or in a two-phase launch after phase 0), so
+    // the first npre1 stages of the phase-1 items are never skipped: their
+    // activations are then zero and the products add nothing.  Every role
+    // computes the same npre and npre1.
+    int npre = 0, npre1 = 0;
+    for (int k = 0; k < nmine; ++k) {
+        const Item it = locate_item(sseg, nseg, span.at(k));
+        const int ns = (it.kb1 - it.kb0) / KB_STAGE;
+        npre += ns;
+        if (span.at(k) >= n0) npre1 += ns;
+    }
+    npre = p.prefetch ? min(npre, S) : 0;
+    npre1 = min(npre1, S);
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.maps[i]);
-        if (p.prefetch) {
-            const uint64_t polW = policy_evict_first();
-            for (int i = i_begin; i < i_end && npre < S; ++i) {
-                const Item it = locate_item(sseg, nseg, i);
-                const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
-                const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
-                for (int kb = it.kb0; kb < it.kb1 && npre < S; kb += KB_STAGE, ++npre) {
-                    mbar_expect_tx(&full[npre], W_STAGE_BYTES + XB);
-                    tma_load_3d(sW + (size_t)npre * W_STAGE_BYTES, wm, &full[npre], 0, 0, tb + kb, polW);
-                }
+        const uint64_t polW = policy_evict_first();
+        int w = 0;
+        for (int k = 0; k < nmine && w < npre; ++k) {
+            const Item it = locate_item(sseg, nseg, span.at(k));
+            const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
+            const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
+            for (int kb = it.kb0; kb < it.kb1 && w < npre; kb += KB_STAGE, ++w) {
+                mbar_expect_tx(&full[w], W_STAGE_BYTES + XB);
+                tma_load_3d(sW + (size_t)w * W_STAGE_BYTES, wm, &full[w], 0, 0, tb + kb, polW);
             }
         }
     }
@@ -109,35 +167,92 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             pdl_launch();
             tl_release(p.tl);
             bool ok = true;
-            if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
-            int q = 0;  // stage sequence number
-            for (int i = i_begin; i < i_end && ok; ++i) {
+            bool dep_ok = n0 == 0, flags_ok = !has_skip;
+            // phase-1 stages whose weights are requested but whose activations
+            // wait for phase 0 (at most S of them: the ring)
+            int pend_kb[8], pend_s[8], pend_st[8], npend = 0;
+            auto load_x = [&](int s_, int kb, int st) {
+                const CUtensorMap *xm = &p.maps[sseg[s_].xmap];
+                if (sseg[s_].x3) {
+                    tma_load_3d(sX + (size_t)st * XB, xm, &full[st], 0, 0, kb, polX);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < KB_STAGE; ++h)
+                        tma_load_2d(sX + (size_t)st * XB + (size_t)h * XKB, xm, &full[st], (kb + h) * GEMM_TILE_K, 0,
+                                    polX);
+                }
+            };
+            // wait for phase 0, then release the pending activation copies
+            auto resolve = [&]() -> bool {
+                if (!dep_ok) {
+                    if (!wait_count(p.dep, (uint32_t)n0, abort_flag)) return false;
+                    fence_proxy_async_global();  // phase 0 wrote them through the generic proxy
+                    dep_ok = true;
+                }
+                for (int j = 0; j < npend; ++j) load_x(pend_s[j], pend_kb[j], pend_st[j]);
+                npend = 0;
+                return true;
+            };
+            int q = 0;   // stage sequence number
+            int w = 0;   // walk index (skipped stages included)
+            int w1 = 0;  // walk index among phase-1 stages
+            for (int k = 0; k < nmine && ok; ++k) {
+                const int i = span.at(k);
+                const bool ph1 = i >= n0;
                 const Item it = locate_item(sseg, nseg, i);
                 const int tb = sseg[it.s].tile_base + it.tile * sseg[it.s].kb;
                 const CUtensorMap *wm = &p.maps[sseg[it.s].wmap];
-                const CUtensorMap *xm = &p.maps[sseg[it.s].xmap];
                 for (int kb = it.kb0; kb < it.kb1; kb += KB_STAGE) {
-                    if (stage_skipped(skip, kb)) continue;
+                    ++w;
+                    if (ph1) {
+                        const bool skippable = has_skip && w1 >= npre1;
+                        ++w1;
+                        if (skippable) {
+                            if (!flags_ok) {  // the flags are staged once phase 0 is complete
+                                if (!resolve() || !mbar_wait(&flags_ready, 0u, abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                flags_ok = true;
+                            }
+                            if (stage_skipped(skip, kb)) continue;
+                        }
+                    }
                     const int st = q % S;
                     if (q >= npre) {
-                        if (q >= S && !mbar_wait(&empty[st], (uint32_t)((q / S) - 1) & 1u, abort_flag)) {
-                            ok = false;
-                            break;
+                        if (q >= S) {
+                            if (npend == S && !resolve()) {  // the ring holds only pending stages
+                                ok = false;
+                                break;
+                            }
+                            if (!mbar_wait(&empty[st], (uint32_t)((q / S) - 1) & 1u, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
                         }
                         mbar_expect_tx(&full[st], W_STAGE_BYTES + XB);
                         tma_load_3d(sW + (size_t)st * W_STAGE_BYTES, wm, &full[st], 0, 0, tb + kb, polW);
                     }  // else: the weights were requested before the dependency wait
-                    if (sseg[it.s].x3) {
-                        tma_load_3d(sX + (size_t)st * XB, xm, &full[st], 0, 0, kb, polX);
+                    if (ph1 && !dep_ok && check_count(p.dep, (uint32_t)n0)) {
+                        fence_proxy_async_global();
+                        dep_ok = true;
+                    }
+                    if (ph1 && !dep_ok) {
+                        pend_kb[npend] = kb;
+                        pend_s[npend] = it.s;
+                        pend_st[npend] = st;
+                        ++npend;
                     } else {
-#pragma unroll
-                        for (int h = 0; h < KB_STAGE; ++h)
-                            tma_load_2d(sX + (size_t)st * XB + (size_t)h * XKB, xm, &full[st], (kb + h) * GEMM_TILE_K,
-                                        0, polX);
+                        if (npend && !resolve()) {
+                            ok = false;
+                            break;
+                        }
+                        load_x(it.s, kb, st);
                     }
                     ++q;
                 }
             }
+            if (ok && npend && !resolve()) ok = false;
             if (!ok) {
                 *abort_flag = 1u;
                 atomicOr(p.err, ERR_TIMEOUT);
@@ -150,10 +265,11 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(GEMM_TILE_M, npad);
-            bool ok = true;
-            if (has_skip && !mbar_wait(&flags_ready, 0u, abort_flag)) ok = false;
-            int q = 0, n = 0;
-            for (int i = i_begin; i < i_end && ok; ++i, ++n) {
+            bool ok = true, flags_ok = !has_skip;
+            int q = 0, n = 0, w1 = 0;
+            for (int k = 0; k < nmine && ok; ++k, ++n) {
+                const int i = span.at(k);
+                const bool ph1 = i >= n0;
                 const Item it = locate_item(sseg, nseg, i);
                 const int buf = n % NB;
                 if (n >= NB && !mbar_wait(&acc_empty[buf], (uint32_t)((n / NB) - 1) & 1u, abort_flag)) {
@@ -164,7 +280,20 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
                 const uint32_t d_tmem = tmem + (uint32_t)(buf * npad);
                 uint32_t issued = 0;
                 for (int kb = it.kb0; kb < it.kb1; kb += KB_STAGE) {
-                    if (stage_skipped(skip, kb)) continue;
+                    if (ph1) {
+                        const bool skippable = has_skip && w1 >= npre1;
+                        ++w1;
+                        if (skippable) {
+                            if (!flags_ok) {
+                                if (!mbar_wait(&flags_ready, 0u, abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                flags_ok = true;
+                            }
+                            if (stage_skipped(skip, kb)) continue;
+                        }
+                    }
                     const int st = q % S;
                     if (!mbar_wait(&full[st], (uint32_t)(q / S) & 1u, abort_flag)) {
                         ok = false;
@@ -193,29 +322,51 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..17)
         pdl_wait();
         const int qd = warp & 3;              // TMEM lane quarter of this warp
         const int row = qd * 32 + lane;       // accumulator row = weight row within the tile
         const int et = threadIdx.x - 64;      // 0..EPI_THREADS-1
         const int grp = et >> 7;              // column-chunk group within the lane quarter
         uint32_t *nz_out = p.nz_out;
-        if (has_skip) {  // stage the k-block flags written by the preceding kernel
-            const int nkb = sseg[0].kb < MAX_NZ_BLOCKS ? sseg[0].kb : MAX_NZ_BLOCKS;  // padded count
-            const int nreal = (sseg[0].K + GEMM_TILE_K - 1) / GEMM_TILE_K;             // flags written
-            for (int j = et; j < nkb; j += EPI_THREADS) snz[j] = j < nreal ? p.nz_skip[j] : 0u;
-            named_bar(1, EPI_THREADS);
-            if (et == 0) mbar_arrive(&flags_ready);
-        }
-        int n = 0;
-        for (int i = i_begin; i < i_end; ++i, ++n) {
+        bool ph1_ready = false;  // phase 0 complete and the sparsity flags staged
+        int n = 0, w1 = 0;
+        for (int k = 0; k < nmine; ++k, ++n) {
+            const int i = span.at(k);
+            const bool ph1 = i >= n0;
+            if (ph1 && !ph1_ready) {
+                if (n0 > 0) {  // wait for every phase-0 item (all CTAs) to be stored
+                    if (et == 0) s_ok = wait_count(p.dep, (uint32_t)n0, abort_flag) ? 1u : 0u;
+                    named_bar(3, EPI_THREADS);
+                    const bool ok_dep = s_ok != 0u;
+                    named_bar(3, EPI_THREADS);
+                    if (!ok_dep) {
+                        if (et == 0) {
+                            *abort_flag = 1u;
+                            atomicOr(p.err, ERR_TIMEOUT);
+                        }
+                        break;
+                    }
+                }
+                if (has_skip) {  // stage the k-block flags of the skipping segment
+                    const GemmSeg &ks = sseg[p.skip_seg];
+                    const int nkb = ks.kb < MAX_NZ_BLOCKS ? ks.kb : MAX_NZ_BLOCKS;  // padded count
+                    const int nreal = (ks.K + GEMM_TILE_K - 1) / GEMM_TILE_K;     // flags written
+                    for (int j = et; j < nkb; j += EPI_THREADS) snz[j] = j < nreal ? __ldcg(p.nz_skip + j) : 0u;
+                    named_bar(1, EPI_THREADS);
+                    if (et == 0) mbar_arrive(&flags_ready);
+                }
+                ph1_ready = true;
+            }
             const Item it = locate_item(sseg, nseg, i);
             const GemmSeg sg = sseg[it.s];  // register copy
             const int buf = n % NB;
-            bool valid = false;
-            for (int kb = it.kb0; kb < it.kb1; kb += KB_STAGE)
-                if (!stage_skipped(skip, kb)) valid = true;
-            // thread 0 waits and tells the others, so that all 128 threads take
+            bool valid = !ph1;
+            for (int kb = it.kb0; kb < it.kb1 && ph1; kb += KB_STAGE)
+                if (w1++ < npre1 || !has_skip || !stage_skipped(skip, kb)) valid = true;
+            const int nrow = it.tile * GEMM_TILE_M + row;
+            const float bias = epi_bias(sg, nrow);  // in flight while the accumulator fills
+            // thread 0 waits and tells the others, so that all threads take
             // the same path through the named barriers below
             if (et == 0) s_ok = mbar_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u, abort_flag) ? 1u : 0u;
             named_bar(3, EPI_THREADS);
@@ -231,8 +382,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             (void)mbar_try_wait(&acc_full[buf], (uint32_t)(n / NB) & 1u);
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * npad);
-            const int nrow = it.tile * GEMM_TILE_M + row;
-            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B, grp * EPI_CW);
+            const bool nzany = epi_item(sseg[it.s], taddr, valid, nrow, it.split, npad, B, grp * EPI_CW, bias);
             tc_fence_before();
             mbar_arrive(&acc_empty[buf]);
             if (sg.epi == EPI_RELU2 && sg.S == 1 && nz_out != nullptr) {
@@ -250,6 +400,13 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
                     if (p.nz_count && nnz) atomicAdd(p.nz_count, nnz);
                 }
                 named_bar(2, EPI_THREADS);
+            }
+            if (!ph1) {  // a phase-0 item is stored: count it (release)
+                named_bar(3, EPI_THREADS);
+                if (et == 0) {
+                    __threadfence();
+                    atomicAdd(p.dep, 1u);
+                }
             }
         }
     }

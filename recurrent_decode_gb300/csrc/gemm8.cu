@@ -336,7 +336,8 @@ __global__ void __launch_bounds__(GEMM_TC8_THREADS, 1) gemm_tc8_kernel(const __g
             tc_fence_after();
             const uint32_t taddr = tmem + tlane + (uint32_t)(buf * npad);
             const int nrow = it.tile * GEMM_TILE_M + row;
-            const bool nzany = epi_item(sg, taddr, valid, nrow, it.split, npad, B, grp * EPI_CW);
+            const bool nzany = epi_item(sseg[it.s], taddr, valid, nrow, it.split, npad, B, grp * EPI_CW,
+                                        epi_bias(sseg[it.s], nrow));
             tc_fence_before();
             mbar_arrive(&acc_empty[buf]);
             if (sg.epi == EPI_RELU2 && sg.S == 1 && nz_out != nullptr) {
@@ -379,15 +380,12 @@ size_t gemm_tc8_smem_bytes(int npad, int kbs, int stages_w, int stages_x) {
 }
 
 void launch_gemm_tc8(const GemmParams &p, int grid, size_t smem, const LaunchCfg &lc, cudaError_t *e) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t r = cudaFuncSetAttribute(gemm_tc8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             gemm_tc_max_smem());
+    {
+        cudaError_t r = ensure_smem_attr((const void *)gemm_tc8_kernel, gemm_tc_max_smem());
         if (r != cudaSuccess) {
             *e = r;
             return;
         }
-        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

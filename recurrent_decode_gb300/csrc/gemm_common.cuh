@@ -71,10 +71,8 @@ __device__ __forceinline__ void chunk_ld(uint32_t taddr, float (&v)[32], bool fu
 // TMEM loads (they are warp-collective); stores are guarded.
 template <int KIND>
 __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split, int npad,
-                                        int B, int c0) {
+                                        int B, int c0, float bias) {
     const bool live = n < sg.rows;
-    float bias = 0.0f;
-    if ((KIND == EPI_DECAY || KIND == EPI_SIGMOID_BIAS) && live) bias = __half2float(sg.bias[n]);
     const bool scaled = sg.wscale != nullptr;  // int8 weights: the row sum times the row's scale
     const float wsc = scaled && live ? __half2float(sg.wscale[n]) : 1.0f;
     bool nz = false;
@@ -136,20 +134,30 @@ __device__ __forceinline__ bool epi_run(const GemmSeg &sg, uint32_t taddr, bool 
     return nz;
 }
 
-__device__ __forceinline__ bool epi_item(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split, int npad,
-                                         int B, int c0) {
-    if (sg.S > 1) return epi_run<-1>(sg, taddr, valid, n, split, npad, B, c0);
+// Out of line: one copy of the epilogue code serves every item.  Inlined at
+// each call site the kernel's code grew past what the instruction cache keeps
+// warm between items, and the graph-replayed step ran 2-4 % slower.
+// `bias`: the segment's bias of row n (EPI_DECAY / EPI_SIGMOID_BIAS), loaded
+// by the caller before it waits for the accumulator (see epi_bias).
+static __device__ __noinline__ bool epi_item(const GemmSeg &sg, uint32_t taddr, bool valid, int n, int split,
+                                             int npad, int B, int c0, float bias) {
+    if (sg.S > 1) return epi_run<-1>(sg, taddr, valid, n, split, npad, B, c0, bias);
     switch (sg.epi) {
-        case EPI_F32: return epi_run<EPI_F32>(sg, taddr, valid, n, split, npad, B, c0);
-        case EPI_F16: return epi_run<EPI_F16>(sg, taddr, valid, n, split, npad, B, c0);
-        case EPI_F16_TANH: return epi_run<EPI_F16_TANH>(sg, taddr, valid, n, split, npad, B, c0);
-        case EPI_F16_SIGMOID: return epi_run<EPI_F16_SIGMOID>(sg, taddr, valid, n, split, npad, B, c0);
-        case EPI_DECAY: return epi_run<EPI_DECAY>(sg, taddr, valid, n, split, npad, B, c0);
-        case EPI_SIGMOID_BIAS: return epi_run<EPI_SIGMOID_BIAS>(sg, taddr, valid, n, split, npad, B, c0);
-        case EPI_RESID: return epi_run<EPI_RESID>(sg, taddr, valid, n, split, npad, B, c0);
-        case EPI_RELU2: return epi_run<EPI_RELU2>(sg, taddr, valid, n, split, npad, B, c0);
+        case EPI_F32: return epi_run<EPI_F32>(sg, taddr, valid, n, split, npad, B, c0, bias);
+        case EPI_F16: return epi_run<EPI_F16>(sg, taddr, valid, n, split, npad, B, c0, bias);
+        case EPI_F16_TANH: return epi_run<EPI_F16_TANH>(sg, taddr, valid, n, split, npad, B, c0, bias);
+        case EPI_F16_SIGMOID: return epi_run<EPI_F16_SIGMOID>(sg, taddr, valid, n, split, npad, B, c0, bias);
+        case EPI_DECAY: return epi_run<EPI_DECAY>(sg, taddr, valid, n, split, npad, B, c0, bias);
+        case EPI_SIGMOID_BIAS: return epi_run<EPI_SIGMOID_BIAS>(sg, taddr, valid, n, split, npad, B, c0, bias);
+        case EPI_RESID: return epi_run<EPI_RESID>(sg, taddr, valid, n, split, npad, B, c0, bias);
+        case EPI_RELU2: return epi_run<EPI_RELU2>(sg, taddr, valid, n, split, npad, B, c0, bias);
         default: return false;
     }
+}
+// The bias an epilogue of weight row n needs (0 for kinds without one).
+__device__ __forceinline__ float epi_bias(const GemmSeg &sg, int n) {
+    return (sg.S == 1 && (sg.epi == EPI_DECAY || sg.epi == EPI_SIGMOID_BIAS) && n < sg.rows) ? __half2float(sg.bias[n])
+                                                                                               : 0.0f;
 }
 
 // ---------------------------------------------------------------------------

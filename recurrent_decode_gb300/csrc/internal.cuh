@@ -82,7 +82,19 @@ struct GemmParams {
     const uint32_t *nz_skip;         // nonzero flags per k-block of the activations (or null)
     uint32_t *err;
     unsigned long long *tl;          // timeline words of this launch (measurement only; else null)
+    // Two-phase launch: items [0, n0) (the first segments) are phase 0, spread
+    // over CTAs [0, g0); the rest are phase 1, spread over every CTA, and their
+    // activations -- produced by phase 0 -- are read only once *dep (zero at
+    // launch, counted up per stored phase-0 item) reaches n0.  Every CTA must be
+    // resident at once: the grid is at most one CTA per SM.  n0 = 0: one phase.
+    int n0, g0;
+    uint32_t *dep;
+    int skip_seg;                    // segment whose activations nz_skip describes
 };
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once per
+// (kernel, device, size); thread-safe (a process may drive several devices).
+cudaError_t ensure_smem_attr(const void *kernel, int bytes);
 
 // Launch helpers (implemented in the .cu files).
 struct LaunchCfg {
@@ -175,70 +187,6 @@ struct LoraFinParams {
     unsigned long long *tl;  // timeline words of this launch (measurement only; else null)
 };
 void launch_lora_fin(const LoraFinParams &p, const LaunchCfg &lc, cudaError_t *e);
-
-// ----------------------------------------------------------------------------
-// Persistent decode step: one cooperative kernel (one CTA per SM) runs every
-// layer.  Weight tiles and recurrent states stream through a shared-memory ring
-// regardless of activation readiness; activation operands are loaded once the
-// phase that produces them has signalled completion through a global counter.
-// ----------------------------------------------------------------------------
-constexpr int PK_MAX_SEG = 7;
-constexpr int PK_MAX_MAPS = 40;
-constexpr int PK_NPH = 8;  // counters per layer: LN1, G1, G2, WKV, G3, LN2, G4, G5
-constexpr int PK_S4_MAX = 4;  // k-splits of the channel-mix key projection
-
-struct PkSeg {
-    int wmap, xmap;          // tensor-map indices
-    int x3;                  // 1: xmap is the 3D (col, row, k-block) view, one copy per stage
-    int tiles, kb, rows, S;  // row tiles, k-blocks (padded), output rows, k-splits
-    int layer_tiles;         // weight-map tiles per layer (0: one matrix for all layers)
-    int item0;               // first item of this segment within its phase
-    int epi;                 // final epilogue kind (EPI_*)
-    int fix;                 // 1: output is final (the tile's last split adds the partials);
-                             // 0: raw fp32 partial slabs that the consuming phase adds
-    int cnt0;                // first tile counter of this segment within its layer
-    int ldo;                 // output / slab row stride (elements)
-    void *out;
-    float *part;             // partial slabs [S][bcap][ldo]
-    long long split_stride;  // elements between slabs
-    const __half *bias;      // layer-0 bias vector (EPI_DECAY / EPI_SIGMOID_BIAS)
-    long long bias_stride;   // elements per layer
-};
-struct PkGemm {
-    PkSeg seg[PK_MAX_SEG];
-    int nseg, nitems;
-};
-enum { PKG_G1_0, PKG_G1, PKG_G2_0, PKG_G2, PKG_G3, PKG_G4, PKG_G5, PKG_HEAD, PKG_COUNT };
-
-struct PkParams {
-    CUtensorMap maps[PK_MAX_MAPS];
-    PkGemm g[PKG_COUNT];
-    int nmaps;
-    int B, npad, kbs, stages, ncols, d, H, V, L, n_slots, head;
-    int s3, s5;              // slab counts of the output and value projections
-    long long xstride;       // elements between residual partial slabs (px)
-    int tcnt_layer;          // tile counters per layer
-    const int32_t *slots, *tokens;
-    float *x;                // residual [bcap][d]
-    const __half *emb, *ln0w, *ln0b, *lnow, *lnob;
-    // per-layer vectors: layer-0 pointers, layer l at + l * d
-    const __half *ln1w, *ln1b, *ln2w, *ln2b, *mu[6], *fxk, *k_k, *k_a, *r_k, *lnxw, *lnxb;
-    __half *xmix[6], *xk, *z, *xo;
-    float *r, *k, *v, *dec, *a, *vg, *gate, *vfirst, *px;
-    const float *pr, *pk, *pv;  // r, k, v split-K slabs [s1][bcap][d] (stride xstride)
-    int s1;
-    float *wkv, *shift_att, *shift_ffn;
-    uint32_t *cnt;           // [L * PK_NPH + 2] phase counters (zero at launch)
-    uint32_t *tcnt;          // [(L + 1) * tcnt_layer] tile counters (zero at launch)
-    uint32_t *dup;           // slot bitmap [ceil(n_slots / 32)] (zero at launch)
-    uint32_t *abort_flag;    // set by any CTA that gives up waiting (zero at launch)
-    uint32_t *diag;          // [8] where the first wait gave up (zero at launch)
-    uint32_t *prog;          // [grid][4] last position of each role (zero at launch)
-    uint32_t *err;
-};
-size_t pk_smem_bytes(int npad, int kbs, int stages);
-int pk_max_stages(int npad, int kbs);
-void launch_persistent(const PkParams &p, int grid, size_t smem, cudaStream_t st, cudaError_t *e);
 
 struct SampleParamsDev {  // device copy of one slot's sampling parameters
     float temperature, top_p;

@@ -29,6 +29,27 @@
 
 using namespace rk;
 
+cudaError_t rk::ensure_smem_attr(const void *kernel, int bytes) {
+    // a fixed table (no heap allocation, so the allocation-free sampler path can
+    // use it); when it is full the attribute is simply set again on every call
+    struct Entry {
+        const void *kernel;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int ndone = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < ndone; ++i)
+        if (done[i].kernel == kernel && done[i].dev == dev && done[i].bytes == bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && ndone < 256) done[ndone++] = Entry{kernel, dev, bytes};
+    return e;
+}
+
 namespace {
 
 // ---------------------------------------------------------------- weights
@@ -52,7 +73,7 @@ const char *kind_name[W_COUNT] = {
 
 // kernel classes reported by rwkv7_profile_step
 enum PClass { P_EMBED, P_LN_MIX, P_GEMM_PROJ, P_GEMM_LORA, P_WKV, P_GEMM_OUT, P_GEMM_KEY, P_GEMM_VALUE, P_LN_OUT,
-              P_GEMM_HEAD, P_SAMPLER, P_LORA_FIN, P_COUNT };
+              P_GEMM_HEAD, P_SAMPLER, P_LORA_FIN, P_GEMM_FFN, P_COUNT };
 
 struct Prof {
     std::vector<cudaEvent_t> ev;  // pairs (begin, end)
@@ -129,13 +150,13 @@ struct rwkv7_ctx {
     float *pr = nullptr, *pk = nullptr, *pv = nullptr, *phw = nullptr, *pha = nullptr, *phv = nullptr,
           *phg = nullptr, *px = nullptr;
     uint32_t *errw = nullptr;
+    uint32_t *ffn_dep = nullptr;  // per layer: key-projection items stored (fused channel mix), zeroed per step
     unsigned long long *nzstat = nullptr;  // nonzero channel-mix blocks counted by the key projection
     unsigned long long nz_considered = 0;  // blocks those counts cover (host side)
     // prefill: second residual buffer and WKV work buffers [bcap][d] ([bcap][H] bonus)
     float *x2 = nullptr, *pf_vec = nullptr, *pf_y = nullptr, *pf_bonus = nullptr;
 
     CUtensorMap wmap[W_COUNT]{};
-    CUtensorMap wmap1[W_COUNT]{};  // box of one k-block tile (persistent step with N > 128)
     CUtensorMap wmap8[W_COUNT]{};  // int8 tiles, two k-blocks per copy
     CUtensorMap wmap8_1[W_COUNT]{};  // int8 tiles, one k-block per copy
     bool has_wmap[W_COUNT]{};
@@ -151,12 +172,6 @@ struct rwkv7_ctx {
     // kernel class of each launch of the captured step
     unsigned long long *tlbuf = nullptr;
     std::map<std::tuple<int, int, int>, std::vector<int>> tl_classes;
-    // persistent step: counters (phase, tile, slot bitmap, abort), zeroed per step
-    uint32_t *pkbuf = nullptr;
-    size_t pk_words = 0;
-    int pk_tcnt_layer = 0;
-    float *p4 = nullptr;  // key-projection partial slabs [PK_S4_MAX][bcap][F]
-    std::map<std::pair<int, int>, PkParams> pk_params;
     std::vector<void *> allocs;
     DevAllocator alloc;  // the allocator in effect when the ctx was created
     Prof prof;
@@ -261,10 +276,7 @@ int make_wmap(rwkv7_ctx *c, int kind) {
     uint64_t strides[2] = {(uint64_t)GEMM_TILE_K * 2, (uint64_t)GEMM_TILE_K * GEMM_TILE_M * 2};
     uint32_t box[3] = {64, 128, 2};
     c->has_wmap[kind] = true;
-    int rc = make_map(c, &c->wmap[kind], c->w[kind], 3, dims, strides, box);
-    if (rc) return rc;
-    uint32_t box1[3] = {64, 128, 1};
-    return make_map(c, &c->wmap1[kind], c->w[kind], 3, dims, strides, box1);
+    return make_map(c, &c->wmap[kind], c->w[kind], 3, dims, strides, box);
 }
 
 // Split factor of a launch whose segments hold `tiles` row tiles in all, each
@@ -338,11 +350,23 @@ struct Seg {
     int S;        // k-splits (S > 1: raw fp32 partials, slab stride bcap * ldo)
 };
 
+// The channel mix runs as one two-phase launch (key projection, then the value
+// projection on every SM once all of h is stored) in the fp16 tensor-core
+// modes; otherwise as two launches.
+bool ffn_fused(const rwkv7_ctx *c, int mode) {
+    return c->wbits == 16 && (mode == 0 || mode == 1) && env_int("RWKV7_FUSE_FFN", 1) != 0;  // tuning knob
+}
+
+// nseg0 > 0: a two-phase launch whose first nseg0 segments are phase 0 and
+// whose phase-1 activations wait for them through the counter *dep (fp16
+// tensor-core kernel only).
 int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *nz_out, const uint32_t *nz_skip,
-             const LaunchCfg &lc, int mode, unsigned long long *tl = nullptr) {
+             const LaunchCfg &lc, int mode, unsigned long long *tl = nullptr, int nseg0 = 0,
+             uint32_t *dep = nullptr) {
     GemmParams p;
     memset(&p, 0, sizeof p);
     p.tl = tl;
+    p.skip_seg = n - 1;
     p.nz_count = nz_out ? c->nzstat : nullptr;
     int nmaps = 0;
     int wslot[W_COUNT], aslot[A_COUNT];
@@ -401,6 +425,7 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
             g.item0 = item;
             item += g.tiles * g.S;
         }
+        if (s + 1 == nseg0) p.n0 = item;  // phase-0 items: those of the first nseg0 segments
     }
     p.nseg = n;
     p.nmaps = nmaps;
@@ -450,8 +475,18 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         // has its SM to itself (its shared memory is over half of the SM's),
         // so it may take all of them.
         p.accbufs = (2 * p.npad * per_sm <= 512) ? 2 : 1;
-        p.prefetch = nz_skip == nullptr ? 1 : 0;
-        const int grid = std::min(p.nitems, c->nsm * per_sm);
+        // weights fetched before the dependency wait, except by a launch that
+        // skips stages by flags its predecessor writes (in a two-phase launch
+        // only the first phase-1 stages are fetched regardless of the flags)
+        p.prefetch = (nz_skip == nullptr || nseg0 > 0) ? 1 : 0;
+        int grid = std::min(p.nitems, c->nsm * per_sm);
+        if (nseg0 > 0) {  // every CTA resident at once: one per SM
+            if (!dep || mode == 2 || w8) return fail(c, RWKV7_ECUDA, "internal: two-phase launch");
+            p.dep = dep;
+            p.g0 = std::min(p.n0, c->nsm);
+            grid = std::min(c->nsm, std::max(p.g0, p.nitems - p.n0));
+            p.accbufs = (2 * p.npad <= 512) ? 2 : 1;
+        }
         launch_gemm_tc(p, grid, gemm_tc_smem_bytes(p.npad, stages), lc, &e);
     }
     if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "GEMM launch: %s", cudaGetErrorString(e));
@@ -509,6 +544,11 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     ep.emb = c->w[W_EMB];
     ep.ln_w = c->w[W_LN0W];
     ep.ln_b = c->w[W_LN0B];
+    const bool fuse_ffn = ffn_fused(c, mode);
+    if (fuse_ffn) {  // the per-layer counters of the fused channel mix start at zero every step
+        e = cudaMemsetAsync(c->ffn_dep, 0, (size_t)c->L * 4, st);
+        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "counter reset: %s", cudaGetErrorString(e));
+    }
     pb(P_EMBED);
     ep.tl = tlp(P_EMBED);
     launch_embed(ep, lc0, &e);
@@ -645,15 +685,22 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
         // G4: key + ReLU^2 (+ nonzero flags per 64 hidden units)
-        Seg g4[1] = {{L_FK, A_XKF, c->xk, d, EPI_RELU2, c->h, c->F, nullptr, 1}};
-        pb(P_GEMM_KEY);
-        if ((rc = run_gemm(c, l, g4, 1, B, c->nz, nullptr, lc, mode, tlp(P_GEMM_KEY)))) return rc;
-        pe();
-        // G5: value over the nonzero hidden blocks, as residual partial slabs
-        Seg g5[1] = {{L_FV, A_H, c->h, c->F, EPI_F32, c->px, d, nullptr, s5}};
-        pb(P_GEMM_VALUE);
-        if ((rc = run_gemm(c, l, g5, 1, B, nullptr, c->nz, lc, mode, tlp(P_GEMM_VALUE)))) return rc;
-        pe();
+        Seg g4[2] = {{L_FK, A_XKF, c->xk, d, EPI_RELU2, c->h, c->F, nullptr, 1},
+                     // G5: value over the nonzero hidden blocks, as residual partial slabs
+                     {L_FV, A_H, c->h, c->F, EPI_F32, c->px, d, nullptr, s5}};
+        if (fuse_ffn) {
+            pb(P_GEMM_FFN);
+            if ((rc = run_gemm(c, l, g4, 2, B, c->nz, c->nz, lc, mode, tlp(P_GEMM_FFN), 1, c->ffn_dep + l)))
+                return rc;
+            pe();
+        } else {
+            pb(P_GEMM_KEY);
+            if ((rc = run_gemm(c, l, g4, 1, B, c->nz, nullptr, lc, mode, tlp(P_GEMM_KEY)))) return rc;
+            pe();
+            pb(P_GEMM_VALUE);
+            if ((rc = run_gemm(c, l, g4 + 1, 1, B, nullptr, c->nz, lc, mode, tlp(P_GEMM_VALUE)))) return rc;
+            pe();
+        }
         px_splits = s5;
     }
     if (head) {
@@ -697,231 +744,11 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     return RWKV7_OK;
 }
 
-// ---------------------------------------------------------------- persistent step
-// k-splits of a phase with `tiles` row tiles of `units` ring stages each: the
-// smallest per-CTA load, counting about 1.5 stages of fixed cost per item and a
-// little per split.
-int pk_split(const rwkv7_ctx *c, int tiles, int units, int max_s) {
-    int best = 1;
-    double best_cost = 1e30;
-    for (int s = 1; s <= std::min(max_s, units); ++s) {
-        const int per_cta = (tiles * s + c->nsm - 1) / c->nsm;
-        const double cost = per_cta * ((units + s - 1) / s + 1.5) + (s > 1 ? 0.25 * s : 0.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = s;
-        }
-    }
-    return best;
-}
-
-int build_pk(rwkv7_ctx *c, int B, bool head, PkParams **out) {
-    auto key = std::make_pair(B, (int)head);
-    auto found = c->pk_params.find(key);
-    if (found != c->pk_params.end()) {
-        *out = &found->second;
-        return RWKV7_OK;
-    }
-    PkParams p;
-    memset(&p, 0, sizeof p);
-    const int d = c->d;
-    p.npad = (B + 15) / 16 * 16;
-    p.kbs = p.npad <= 128 ? 2 : 1;
-    p.stages = pk_max_stages(p.npad, p.kbs);
-    if (p.stages < 2) return fail(c, RWKV7_ECUDA, "persistent step: shared memory too small");
-    int ncols = 32;
-    while (ncols < 2 * p.npad) ncols <<= 1;
-    p.ncols = ncols;
-    if (d > 4096) return fail(c, RWKV7_EINVAL, "persistent step supports d_model <= 4096");
-    int wslot[W_COUNT], aslot[A_COUNT];
-    for (int i = 0; i < W_COUNT; ++i) wslot[i] = -1;
-    for (int i = 0; i < A_COUNT; ++i) aslot[i] = -1;
-    int nmaps = 0;
-    auto wmap_of = [&](int kind) -> int {
-        if (wslot[kind] < 0) {
-            if (nmaps >= PK_MAX_MAPS) return -1;
-            wslot[kind] = nmaps;
-            p.maps[nmaps++] = p.kbs == 2 ? c->wmap[kind] : c->wmap1[kind];
-        }
-        return wslot[kind];
-    };
-    bool x3of[A_COUNT] = {};
-    auto amap_of = [&](int which) -> int {
-        if (aslot[which] < 0) {
-            if (nmaps >= PK_MAX_MAPS) return -1;
-            const CUtensorMap *am3 = p.kbs == 2 ? get_amap3(c, which, p.npad) : nullptr;
-            const CUtensorMap *am = am3 ? am3 : get_amap(c, which, p.npad);
-            if (!am) return -1;
-            aslot[which] = nmaps;
-            x3of[which] = am3 != nullptr;
-            p.maps[nmaps++] = *am;
-        }
-        return aslot[which];
-    };
-    const int G = c->nsm;
-    const int units = kblocks(c, L_WR) / p.kbs;
-    const int g1_tiles = 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) + row_tiles(c, L_V1) +
-                         row_tiles(c, L_G1);
-    const int s1 = pk_split(c, g1_tiles, units, MAX_SPLIT);
-    const int s3 = pk_split(c, row_tiles(c, L_WO), kblocks(c, L_WO) / p.kbs, MAX_SPLIT);
-    const int s5 = pk_split(c, row_tiles(c, L_FV), kblocks(c, L_FV) / p.kbs, MAX_SPLIT);
-    const long long xs = (long long)c->bcap;
-    int cnt0 = 0;
-    bool bad_map = false;
-    auto add = [&](PkGemm &g, int kind, int abuf, int epi, int fix, void *outp, int ldo, float *part,
-                   const __half *bias, int S) {
-        PkSeg &sg = g.seg[g.nseg++];
-        sg.wmap = wmap_of(kind);
-        sg.xmap = amap_of(abuf);
-        if (sg.wmap < 0 || sg.xmap < 0) bad_map = true;
-        sg.x3 = (sg.xmap >= 0 && x3of[abuf]) ? 1 : 0;
-        sg.tiles = row_tiles(c, kind);
-        sg.kb = kblocks(c, kind);
-        sg.rows = c->wrows[kind];
-        sg.S = std::max(1, std::min(S, sg.kb / p.kbs));
-        sg.layer_tiles = per_layer(kind) ? sg.tiles * sg.kb : 0;
-        sg.item0 = g.nitems;
-        g.nitems += sg.tiles * sg.S;
-        sg.epi = epi;
-        sg.fix = fix;
-        sg.cnt0 = 0;
-        if (fix && sg.S > 1) {
-            sg.cnt0 = cnt0;
-            cnt0 += sg.tiles;
-        }
-        sg.ldo = ldo;
-        sg.out = outp;
-        sg.part = part;
-        sg.split_stride = xs * ldo;
-        sg.bias = bias;
-        sg.bias_stride = d;
-    };
-    for (int v1 = 0; v1 < 2; ++v1) {  // layer 0 has no value LoRA
-        PkGemm &g = p.g[v1 ? PKG_G1 : PKG_G1_0];
-        cnt0 = 0;
-        add(g, L_WR, A_XR, EPI_F32, 0, nullptr, d, c->pr, nullptr, s1);  // slabs, added by the WKV phase
-        add(g, L_WK, A_XK, EPI_F32, 0, nullptr, d, c->pk, nullptr, s1);
-        add(g, L_WV, A_XV, EPI_F32, 0, nullptr, d, c->pv, nullptr, s1);
-        // LoRA-down outputs feed the next GEMM's operand loads, so they are
-        // produced whole (no split) with their activation applied
-        add(g, L_W1, A_XW, EPI_F16_TANH, 1, c->hw, c->rw, c->phw, nullptr, 1);
-        add(g, L_A1, A_XA, EPI_F16, 1, c->ha, c->ra, c->pha, nullptr, 1);
-        if (v1) add(g, L_V1, A_XV, EPI_F16, 1, c->hv, c->rv, c->phv, nullptr, 1);
-        add(g, L_G1, A_XG, EPI_F16_SIGMOID, 1, c->hg, c->rg, c->phg, nullptr, 1);
-        PkGemm &g2 = p.g[v1 ? PKG_G2 : PKG_G2_0];
-        add(g2, L_W2, A_HW, EPI_DECAY, 1, c->dec, d, nullptr, c->w[L_W0], 1);
-        add(g2, L_A2, A_HA, EPI_SIGMOID_BIAS, 1, c->a, d, nullptr, c->w[L_A0], 1);
-        if (v1) add(g2, L_V2, A_HV, EPI_SIGMOID_BIAS, 1, c->vg, d, nullptr, c->w[L_V0], 1);
-        add(g2, L_G2, A_HG, EPI_F32, 1, c->g, d, nullptr, nullptr, 1);
-    }
-    const int g1cnt = cnt0;
-    add(p.g[PKG_G3], L_WO, A_Z, EPI_F32, 0, nullptr, d, c->px, nullptr, s3);
-    cnt0 = g1cnt;
-    add(p.g[PKG_G4], L_FK, A_XKF, EPI_RELU2, 1, c->h, c->F, c->p4, nullptr, env_int("RWKV7_PK_S4", 1));
-    add(p.g[PKG_G5], L_FV, A_H, EPI_F32, 0, nullptr, d, c->px, nullptr, s5);
-    cnt0 = 0;
-    add(p.g[PKG_HEAD], W_HEAD, A_XO, EPI_F32, 1, c->logits, c->V, nullptr, nullptr, 1);
-    if (bad_map) return fail(c, RWKV7_ECUDA, "persistent step: tensor maps");
-    if (cnt0 > c->pk_tcnt_layer && false) return fail(c, RWKV7_ECUDA, "internal: tile counters");
-    p.nmaps = nmaps;
-    p.B = B;
-    p.d = d;
-    p.H = c->H;
-    p.V = c->V;
-    p.L = c->L;
-    p.n_slots = c->n_slots;
-    p.head = head ? 1 : 0;
-    p.s3 = p.g[PKG_G3].seg[0].S;
-    p.s5 = p.g[PKG_G5].seg[0].S;
-    p.s1 = p.g[PKG_G1].seg[0].S;
-    p.pr = c->pr;
-    p.pk = c->pk;
-    p.pv = c->pv;
-    p.xstride = xs * d;
-    p.tcnt_layer = c->pk_tcnt_layer;
-    p.slots = c->slots;
-    p.tokens = c->tokens;
-    p.x = c->x;
-    p.emb = c->w[W_EMB];
-    p.ln0w = c->w[W_LN0W];
-    p.ln0b = c->w[W_LN0B];
-    p.lnow = c->w[W_LNOW];
-    p.lnob = c->w[W_LNOB];
-    p.ln1w = c->w[L_LN1W];
-    p.ln1b = c->w[L_LN1B];
-    p.ln2w = c->w[L_LN2W];
-    p.ln2b = c->w[L_LN2B];
-    const int mk[6] = {L_XR, L_XW, L_XK, L_XV, L_XA, L_XG};
-    for (int q = 0; q < 6; ++q) {
-        p.mu[q] = c->w[mk[q]];
-        p.xmix[q] = c->xmix[q];
-    }
-    p.fxk = c->w[L_FXK];
-    p.k_k = c->w[L_KK];
-    p.k_a = c->w[L_KA];
-    p.r_k = c->w[L_RK];
-    p.lnxw = c->w[L_LNXW];
-    p.lnxb = c->w[L_LNXB];
-    p.xk = c->xk;
-    p.z = c->z;
-    p.xo = c->xo;
-    p.r = c->r;
-    p.k = c->k;
-    p.v = c->v;
-    p.dec = c->dec;
-    p.a = c->a;
-    p.vg = c->vg;
-    p.gate = c->g;
-    p.vfirst = c->vfirst;
-    p.px = c->px;
-    p.wkv = c->wkv;
-    p.shift_att = c->shift_att;
-    p.shift_ffn = c->shift_ffn;
-    p.cnt = c->pkbuf;
-    p.tcnt = p.cnt + (size_t)c->L * PK_NPH + 2;
-    p.dup = p.tcnt + (size_t)c->L * c->pk_tcnt_layer + row_tiles(c, W_HEAD);
-    p.abort_flag = p.dup + (c->n_slots + 31) / 32;
-    p.diag = p.abort_flag + 1;
-    p.prog = p.diag + 8;
-    p.err = c->errw;
-    (void)G;
-    *out = &c->pk_params.emplace(key, p).first->second;
-    return RWKV7_OK;
-}
-
-int run_persistent(rwkv7_ctx *c, int B, bool head, bool sample) {
-    PkParams *pp = nullptr;
-    int rc = build_pk(c, B, head, &pp);
-    if (rc) return rc;
-    CK(cudaMemsetAsync(c->pkbuf, 0, c->pk_words * 4, c->stream));
-    cudaError_t e = cudaSuccess;
-    launch_persistent(*pp, c->nsm, pk_smem_bytes(pp->npad, pp->kbs, pp->stages), c->stream, &e);
-    if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "persistent step launch: %s", cudaGetErrorString(e));
-    if (head && sample) {
-        SamplerParams sp;
-        memset(&sp, 0, sizeof sp);
-        sp.B = B;
-        sp.V = c->V;
-        sp.n_slots = c->n_slots;
-        sp.slots = c->slots;
-        sp.logits = c->logits;
-        sp.occ = c->occ;
-        sp.params = c->params;
-        sp.ndraw = c->ndraw;
-        sp.lpen = c->lpen;
-        sp.next = c->next;
-        sp.err = c->errw;
-        launch_sampler(sp, LaunchCfg{c->stream, false}, &e);
-        if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "sampler launch: %s", cudaGetErrorString(e));
-    }
-    return RWKV7_OK;
-}
-
 // ---------------------------------------------------------------- chunked prefill
 // n consecutive tokens of one slot (tokens in c->tokens): the tokens form the
 // N side of every projection, so each weight is streamed once per chunk.
 int enqueue_prefill(rwkv7_ctx *c, cudaStream_t st, int slot, int n, bool head) {
-    const int mode = c->mode == 3 ? 0 : c->mode;
+    const int mode = c->mode;
     LaunchCfg lc{st, mode != 2};
     LaunchCfg lc0{st, false};
     cudaError_t e = cudaSuccess;
@@ -1098,7 +925,6 @@ int step_graph(rwkv7_ctx *c, int B, bool head, bool sample, bool timeline, cudaG
 }
 
 int run_step(rwkv7_ctx *c, int B, bool head, bool sample) {
-    if (c->mode == 3) return run_persistent(c, B, head, sample);
     c->nz_considered += (unsigned long long)c->L * ((c->F + 63) / 64);
     if (c->mode != 0) return enqueue_step(c, c->stream, B, head, sample, c->mode);
     cudaGraphExec_t ex = nullptr;
@@ -1265,18 +1091,11 @@ int rwkv7_create_ex(const rwkv7_config *cfg, int32_t weight_bits, void *cuda_str
         (rc = dalloc(c, &c->phg, SR * c->rg)))
         return bad(rc);
     if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
+    if ((rc = dalloc(c, &c->ffn_dep, (size_t)L))) return bad(rc);
     if ((rc = dalloc(c, &c->nzstat, 4))) return bad(rc);
     if ((rc = dalloc(c, &c->x2, R * d)) || (rc = dalloc(c, &c->pf_vec, R * 6 * (size_t)d)) ||
         (rc = dalloc(c, &c->pf_y, R * d)) || (rc = dalloc(c, &c->pf_bonus, R * c->H)))
         return bad(rc);
-    {
-        const int tl = 3 * row_tiles(c, L_WR) + row_tiles(c, L_W1) + row_tiles(c, L_A1) + row_tiles(c, L_V1) +
-                       row_tiles(c, L_G1) + row_tiles(c, L_FK);
-        c->pk_tcnt_layer = tl;
-        c->pk_words = (size_t)L * PK_NPH + 2 + (size_t)L * tl + row_tiles(c, W_HEAD) + (c->n_slots + 31) / 32 + 1 + 8 + 4 * (size_t)c->nsm;
-        if ((rc = dalloc(c, &c->pkbuf, c->pk_words))) return bad(rc);
-        if ((rc = dalloc(c, &c->p4, (size_t)PK_S4_MAX * R * F))) return bad(rc);
-    }
     const int mk[6] = {A_XR, A_XW, A_XK, A_XV, A_XA, A_XG};
     for (int q = 0; q < 6; ++q)
         if ((rc = make_amap(c, mk[q], c->xmix[q], d))) return bad(rc);
@@ -1644,19 +1463,7 @@ int rwkv7_synchronize(rwkv7_ctx *c) {
     CK(cudaMemcpy(&w, c->errw, 4, cudaMemcpyDeviceToHost));
     if (w) {
         CK(cudaMemset(c->errw, 0, 4));
-        if (w & ERR_TIMEOUT) {
-            uint32_t dg[6] = {0, 0, 0, 0, 0, 0}, pg[4] = {0, 0, 0, 0};
-            if (c->pkbuf) {
-                const size_t off = c->pk_words - 8 - 4 * (size_t)c->nsm;
-                cudaMemcpy(dg, c->pkbuf + off, sizeof dg, cudaMemcpyDeviceToHost);
-                if (dg[1] < (uint32_t)c->nsm)
-                    cudaMemcpy(pg, c->pkbuf + off + 8 + 4 * (size_t)dg[1], sizeof pg, cudaMemcpyDeviceToHost);
-            }
-            return fail(c, RWKV7_ETIMEOUT,
-                        "a bounded wait inside a kernel gave up (flags 0x%x; persistent step: where %u cta %u "
-                        "[%u %u %u %u] progress [%08x %08x %08x %08x])",
-                        w, dg[0], dg[1], dg[2], dg[3], dg[4], dg[5], pg[0], pg[1], pg[2], pg[3]);
-        }
+        if (w & ERR_TIMEOUT) return fail(c, RWKV7_ETIMEOUT, "a bounded wait inside a kernel gave up (flags 0x%x)", w);
         return fail(c, RWKV7_EINVAL, "device-side argument error (flags 0x%x: %s%s%s%s)", w,
                     (w & ERR_SLOT) ? "slot out of range " : "", (w & ERR_TOKEN) ? "token out of range " : "",
                     (w & ERR_DUP) ? "repeated slot " : "", (w & ERR_CONFIG) ? "sampler found no token" : "");
@@ -1666,7 +1473,7 @@ int rwkv7_synchronize(rwkv7_ctx *c) {
 
 int rwkv7_set_mode(rwkv7_ctx *c, int32_t mode) {
     if (!c) return RWKV7_EINVAL;
-    if (mode < 0 || mode > 3) return fail(c, RWKV7_EINVAL, "mode must be 0, 1, 2 or 3");
+    if (mode < 0 || mode > 2) return fail(c, RWKV7_EINVAL, "mode must be 0, 1 or 2");
     if (c->wbits == 8 && mode >= 2)
         return fail(c, RWKV7_EINVAL, "int8 weights run in modes 0 and 1 (tensor-core kernels) only");
     c->mode = mode;
@@ -1678,7 +1485,9 @@ int32_t rwkv7_step_kernel_count(const rwkv7_ctx *c, int32_t B, int32_t with_samp
     const int sub = (B + MAX_B - 1) / MAX_B;
     int s1, s3, s5;
     step_splits(c, &s1, &s3, &s5);
-    const int per_layer = s1 == 1 ? 8 : 9;  // the LoRA finalize kernel runs only for a split r, k, v GEMM
+    // the LoRA finalize kernel runs only for a split r, k, v GEMM; the fused
+    // channel mix is one launch
+    const int per_layer = (s1 == 1 ? 8 : 9) - (ffn_fused(c, c->mode) ? 1 : 0);
     return sub * (1 + per_layer * c->L + 2 + (with_sampling ? 1 : 0));
 }
 

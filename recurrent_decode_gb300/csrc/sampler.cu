@@ -521,15 +521,13 @@ __global__ void __launch_bounds__(SMP_THREADS, 1) sampler_kernel(const SamplerPa
 }
 
 void launch_sampler(const SamplerParams &p, const LaunchCfg &lc, cudaError_t *e) {
-    static bool attr_set = false;
     const size_t smem = sizeof(SmpShared);
-    if (!attr_set) {
-        cudaError_t r = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        cudaError_t r = ensure_smem_attr((const void *)sampler_kernel, (int)smem);
         if (r != cudaSuccess) {
             *e = r;
             return;
         }
-        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.B);

@@ -42,13 +42,25 @@ def assert_logits_close(gpu, ref, what=""):
     return err, cos
 
 
-def greedy_consistent(gpu_token: int, ref_logits) -> bool:
-    """The GPU's greedy token is the oracle's argmax, or within the tolerance of it."""
+# Greedy checks of this test session, and those accepted only by the near-tie
+# rule (oracle margin, where); the summary at the end of the run reports them.
+GREEDY_CHECKS = [0]
+ESCAPES = []
+
+
+def greedy_consistent(gpu_token: int, ref_logits, where: str = "") -> bool:
+    """The GPU's greedy token is the oracle's argmax, or within the tolerance of it
+    (a near tie, counted in ESCAPES with the oracle's margin)."""
+    GREEDY_CHECKS[0] += 1
     ref = np.asarray(ref_logits, np.float64)
     best = int(np.argmax(ref))
     if gpu_token == best:
         return True
-    return ref[best] - ref[gpu_token] <= 2 * LOGIT_ATOL
+    margin = float(ref[best] - ref[gpu_token])
+    if margin <= 2 * LOGIT_ATOL:
+        ESCAPES.append((margin, where))
+        return True
+    return False
 
 
 def oracle_states(weights, dims, n):

@@ -26,3 +26,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """How often a greedy GPU token differed from the oracle's argmax and was
+    accepted as a near tie (within the logit tolerance), with the smallest and
+    largest oracle margin among those cases."""
+    h = sys.modules.get("_harness")
+    if h is None or not h.GREEDY_CHECKS[0]:
+        return
+    esc = h.ESCAPES
+    line = f"greedy token checks: {h.GREEDY_CHECKS[0]}, near-tie escapes: {len(esc)}"
+    if esc:
+        m = [e[0] for e in esc]
+        line += f" (oracle margin min {min(m):.2e}, max {max(m):.2e}; first at {esc[0][1]})"
+    terminalreporter.write_line(line)

@@ -10,8 +10,7 @@ synthetic int8 weights, with the fp16 variant's tolerances.
 - chunked prefill of 300 tokens (a 256-token chunk: N = 256) against the
   oracle's chunked prefill;
 - the channel-mix value projection skipping all-zero blocks (zero key rows);
-- the API refuses fp16 uploads of int8 matrices and the CUDA-core / persistent
-  modes.
+- the API refuses fp16 uploads of int8 matrices and the CUDA-core mode.
 """
 import os
 

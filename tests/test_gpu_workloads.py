@@ -8,9 +8,13 @@
   for all 256 steps, and the oracle's sampler, given the GPU's fp32 logits, the
   same occurrence counts and draw counters, draws the GPU's token every step.
 - The 2.9B and 7.2B shapes at their benchmark batch (64 and 256 slots), in the
-  benchmark's launch configuration (CUDA-graph replay of the fused step):
-  8-token prompts, 4 greedy decode steps; three rows are followed by the
-  oracle, teacher-forced, and checked within the tolerance.
+  benchmark's launch configuration (CUDA-graph replay of the fused step) and
+  sampling (2.9B greedy; 7.2B the adapter's defaults, top_p 0.3, seeded per
+  slot): 8-token prompts, 8 decode steps; three rows are followed by the
+  oracle, teacher-forced, and checked within the tolerance; greedy tokens are
+  the GPU logits' argmax and the oracle's up to near ties, sampled tokens are
+  the oracle sampler's draw on the GPU's logits with the same occurrence counts
+  and draw index.
 
 Tolerances as in _harness: logits max-abs <= 2e-2, cosine >= 0.9999; greedy
 tokens equal to the oracle's argmax unless the oracle's margin is within it.
@@ -85,13 +89,21 @@ def test_full_shape_bench_batch_teacher_forced(shape):
     import recurrent_decode_gb300 as rd
     dev = torch.device("cuda")
     dims = synth.Dims(shape)
-    B = synth.WORKLOADS[shape]["B"]
+    wl = synth.WORKLOADS[shape]
+    B = wl["B"]
     W = synth.make_weights(shape)
     ctx = rd.Rwkv7(dims, B)
     ctx.set_weights(W)
     ctx.set_mode(0)  # the benchmark's configuration: graph replay
+    greedy = bool(wl.get("greedy"))
+    params = []
     for s in range(B):
-        ctx.set_sampling(s, greedy=True)
+        sp = dict(greedy=True) if greedy else dict(
+            temperature=wl["temperature"], top_p=wl["top_p"], top_k=wl["top_k"], presence=wl["presence"],
+            frequency=wl["frequency"], penalty_decay=wl["penalty_decay"], seed=synth.SAMPLING_SEED_BASE + s,
+            greedy=False)
+        ctx.set_sampling(s, **sp)
+        params.append(sp)
     P = 8
     prompts = synth.prompt_tokens(dims.vocab, B, P, seed=31)
     slots = torch.arange(B, dtype=torch.int32, device=dev)
@@ -104,10 +116,11 @@ def test_full_shape_bench_batch_teacher_forced(shape):
     sts = [m.new_state() for _ in tracked]
     for st, s in zip(sts, tracked):
         st.prefill_chunked(prompts[s, :P - 1], want_logits=False)
+    occ = [np.zeros(dims.vocab, np.float32) for _ in tracked]
     cur = dprompts[:, P - 1].contiguous()
     logits = torch.empty(B, dims.vocab, device=dev)
     nxt = torch.empty(B, dtype=torch.int32, device=dev)
-    for step in range(4):
+    for step in range(8):
         ctx.decode_step(slots, cur, logits, nxt)
         ctx.synchronize()
         tok_in = cur.cpu().numpy()
@@ -116,7 +129,11 @@ def test_full_shape_bench_batch_teacher_forced(shape):
         for k, s in enumerate(tracked):
             ref = sts[k].step(int(tok_in[s]))
             assert_logits_close(rows[k], ref, f"{shape} slot {s} step {step}")
-            assert int(got[s]) == int(np.argmax(rows[k]))
-            assert greedy_consistent(int(got[s]), ref)
+            if greedy:
+                assert int(got[s]) == int(np.argmax(rows[k]))
+                assert greedy_consistent(int(got[s]), ref, f"{shape} slot {s} step {step}")
+            else:
+                tok, _ = oracle.sample(rows[k], occ[k], params[s], step)
+                assert tok == int(got[s]), (shape, s, step, tok, int(got[s]))
         cur = nxt.clone()
     ctx.close()

@@ -98,3 +98,41 @@ def test_static_sampler_rejects_a_batch_beyond_its_scratch():
     assert ei.value.code == rd.EINVAL and "exceeds" in str(ei.value)
     torch.cuda.synchronize()
     assert (nxt.cpu().numpy() == -1).all()   # nothing was launched
+
+
+def test_static_sampler_flags_bad_rows_on_a_side_stream():
+    """n_rows larger than B, one row index out of range, the call on a
+    non-default stream: that row gets token 0 and error flag 1; every other row
+    equals rwkv7_sample_batch's token for the same logits and parameters."""
+    torch = pytest.importorskip("torch")
+    import recurrent_decode_gb300 as rd
+    dev = torch.device("cuda")
+    V, B, n_rows = synth.Dims("tiny").vocab, 6, 11  # the comparison context samples V-wide rows
+    params = [dict(CASES[s % len(CASES)], seed=8100 + s) for s in range(n_rows)]
+    table = torch.from_numpy(rd.sampling_table(params)).to(dev)
+    occ = torch.zeros(n_rows, V, dtype=torch.float32, device=dev)
+    ndraw = torch.zeros(n_rows, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows_np = np.array([9, 2, n_rows + 3, 0, 10, 5], np.int32)  # row 2 is out of range
+    rows = torch.from_numpy(rows_np).to(dev)
+    lg = torch.from_numpy(synth.random_logits(B, V, seed=811, scale=2.5)).to(dev)
+    nxt = torch.full((B,), -1, dtype=torch.int32, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    rd.sample_rows_static(lg, rows, occ, table, ndraw, nxt, err, stream=side)
+    side.synchronize()
+    got = nxt.cpu().numpy()
+    assert int(err.item()) & 1
+    assert got[2] == 0
+
+    # the same rows through a context whose slot s carries params[s]
+    ctx = rd.Rwkv7(synth.Dims("tiny"), n_rows)
+    for s, p in enumerate(params):
+        ctx.set_sampling(s, **{**dict(temperature=1.0, top_p=0.3, top_k=0, presence=0.0, frequency=1.0,
+                                      penalty_decay=0.996, greedy=False), **p})
+    good = [i for i in range(B) if rows_np[i] < n_rows]
+    want = torch.empty(len(good), dtype=torch.int32, device=dev)
+    ctx.sample_batch(torch.from_numpy(rows_np[good].copy()).to(dev), lg[good].contiguous(), want)
+    ctx.synchronize()
+    assert np.array_equal(got[good], want.cpu().numpy())
+    ctx.close()
