@@ -350,54 +350,72 @@ def union_sweep(dev, fractions=(1.0, 0.75, 0.5, 0.25, 0.1), n_layer=8, B=64, ste
     """The sparse channel-mix value projection on weights whose key rows are
     zero for a chosen share of the 64-row hidden blocks (every layer, seeded):
     those hidden blocks are zero for every slot, so the value projection skips
-    their 64 rows of the value matrix.  Reports, per union fraction, the value
-    projection's in-graph time per launch, the whole step, and the roofline
-    counting only the union's value rows."""
+    their 64 rows of the value matrix.  Per union fraction: the value
+    projection's in-graph time per launch when it runs as its own launch (the
+    RWKV7_FUSE_FFN=0 configuration), the roofline counting only the union's
+    value rows, and the whole step both that way and with the fused channel mix
+    the library runs by default (whose speculatively fetched first value stages
+    are never skipped)."""
     import torch
     import recurrent_decode_gb300 as rd
     dm = synth.Dims("2.9b", n_layer)
     W = synth.make_weights("2.9b", n_layer=n_layer)
-    ctx = rd.Rwkv7(dm, B)
-    ctx.set_weights(W)
-    for s in range(B):
-        ctx.set_sampling(s, greedy=True)
+    nblk = dm.d_ffn // 64
+    peak, peak_kind = _peaks()
     slots = torch.arange(B, dtype=torch.int32, device=dev)
     tokens = torch.from_numpy(synth.prompt_tokens(dm.vocab, B, 1)[:, 0].copy()).to(dev)
     nxt = torch.empty(B, dtype=torch.int32, device=dev)
-    nblk = dm.d_ffn // 64
-    rng = np.random.default_rng(5)
-    peak, peak_kind = _peaks()
+    res = {}
+    for fused in (False, True):
+        old = os.environ.get("RWKV7_FUSE_FFN")
+        os.environ["RWKV7_FUSE_FFN"] = "1" if fused else "0"  # read when the step graph is captured
+        ctx = rd.Rwkv7(dm, B)
+        ctx.set_weights(W)
+        for s in range(B):
+            ctx.set_sampling(s, greedy=True)
+        rng = np.random.default_rng(5)
+        for f in fractions:
+            keep = np.zeros(nblk, bool)
+            keep[rng.permutation(nblk)[:max(1, round(f * nblk))]] = True
+            for l in range(n_layer):
+                k = W[f"blocks.{l}.ffn.key"].copy()
+                k.reshape(nblk, 64, dm.d_model)[~keep] = 0
+                ctx.set_weight(f"blocks.{l}.ffn.key", k)
+            for _ in range(3):
+                ctx.decode_step(slots, tokens, None, nxt)
+            ctx.synchronize()
+            ctx.ffn_union_stats()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                ctx.decode_step(slots, tokens, None, nxt)
+            e1.record()
+            torch.cuda.synchronize()
+            nz, tot = ctx.ffn_union_stats()
+            ig, _ = in_graph_times(ctx, slots, tokens, with_sampling=False)
+            res[(fused, f)] = (nz / max(1, tot), e0.elapsed_time(e1) / steps, ig)
+        ctx.close()
+        if old is None:
+            os.environ.pop("RWKV7_FUSE_FFN", None)
+        else:
+            os.environ["RWKV7_FUSE_FFN"] = old
     rows = []
     for f in fractions:
-        keep = np.zeros(nblk, bool)
-        keep[rng.permutation(nblk)[:max(1, round(f * nblk))]] = True
-        for l in range(n_layer):
-            k = W[f"blocks.{l}.ffn.key"].copy()
-            k.reshape(nblk, 64, dm.d_model)[~keep] = 0
-            ctx.set_weight(f"blocks.{l}.ffn.key", k)
-        for _ in range(3):
-            ctx.decode_step(slots, tokens, None, nxt)
-        ctx.synchronize()
-        ctx.ffn_union_stats()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            ctx.decode_step(slots, tokens, None, nxt)
-        e1.record()
-        torch.cuda.synchronize()
-        nz, tot = ctx.ffn_union_stats()
-        ig, _ = in_graph_times(ctx, slots, tokens, with_sampling=False)
+        union, step_ms, ig = res[(False, f)]
+        _, step_fused, igf = res[(True, f)]
         v_ms, v_n = ig["gemm_value"]
-        union = nz / max(1, tot)
         vbytes = union * dm.d_model * dm.d_ffn * 2  # value rows of the union, per launch
         rows.append({"union_fraction": union, "value_us_per_launch": 1e3 * v_ms / v_n,
-                     "step_ms": e0.elapsed_time(e1) / steps,
+                     "key_us_per_launch": 1e3 * ig["gemm_key"][0] / ig["gemm_key"][1],
+                     "step_ms": step_ms,
                      "union_roofline_GBps": vbytes / (v_ms / v_n / 1e3) / 1e9,
-                     "union_roofline_frac": vbytes / (v_ms / v_n / 1e3) / 1e9 / peak})
-    ctx.close()
+                     "union_roofline_frac": vbytes / (v_ms / v_n / 1e3) / 1e9 / peak,
+                     "fused_ffn_us_per_launch": 1e3 * igf["gemm_ffn"][0] / igf["gemm_ffn"][1],
+                     "fused_step_ms": step_fused})
     return {"shape": f"2.9b, {n_layer} layers, B={B}", "peak_kind": peak_kind, "points": rows,
-            "note": "ffn.key rows zeroed for (1 - fraction) of the 64-row hidden blocks; value projection time is "
-                    "its in-graph time per launch (rwkv7_step_timeline); the roofline counts union rows only"}
+            "note": "ffn.key rows zeroed for (1 - fraction) of the 64-row hidden blocks; times are in-graph per launch "
+                    "(rwkv7_step_timeline); value_us: the value projection as its own launch; fused: key + value "
+                    "as one launch; the roofline counts union rows only"}
 
 
 def shrink_sweep(ctx, dm, dev, batches=(256, 128, 64, 32, 16, 8, 4, 2, 1), steps=20):

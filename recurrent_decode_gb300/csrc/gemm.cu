@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
         npre += ns;
         if (span.at(k) >= n0) npre1 += ns;
     }
-    npre = p.prefetch ? min(npre, S) : 0;
+    npre = min(min(npre, S), p.prefetch);
     npre1 = min(npre1, S);
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.maps[i]);

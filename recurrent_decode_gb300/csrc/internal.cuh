@@ -76,7 +76,7 @@ struct GemmParams {
     int stages_x;                    // int8 weights: stages of the activation ring
     int kbs;                         // int8 weights: k-blocks per stage (1 or 2); fp16 weights: always 2
     int accbufs;                     // TMEM accumulator buffers (1 or 2)
-    int prefetch;                    // 1: weights may be fetched before the dependency wait
+    int prefetch;                    // weight stages that may be fetched before the dependency wait (0: none)
     uint32_t *nz_out;                // EPI_RELU2: flag per 64 output rows
     unsigned long long *nz_count;    // EPI_RELU2: running count of nonzero 64-row blocks (or null)
     const uint32_t *nz_skip;         // nonzero flags per k-block of the activations (or null)

@@ -478,7 +478,7 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
         // weights fetched before the dependency wait, except by a launch that
         // skips stages by flags its predecessor writes (in a two-phase launch
         // only the first phase-1 stages are fetched regardless of the flags)
-        p.prefetch = (nz_skip == nullptr || nseg0 > 0) ? 1 : 0;
+        p.prefetch = (nz_skip == nullptr || nseg0 > 0) ? env_int("RWKV7_PREFETCH_STAGES", stages) : 0;  // knob
         int grid = std::min(p.nitems, c->nsm * per_sm);
         if (nseg0 > 0) {  // every CTA resident at once: one per SM
             if (!dep || mode == 2 || w8) return fail(c, RWKV7_ECUDA, "internal: two-phase launch");
