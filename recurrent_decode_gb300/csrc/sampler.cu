@@ -200,10 +200,12 @@ __device__ __forceinline__ void hist_add_warp(SmpShared &sm, uint32_t key, uint3
     }
 }
 
-// Two CTAs per SM (32 registers a thread, a few spilled): a batch of up to two
-// rows per SM runs as one wave -- at B=256 one wave of 256 rows took 165 us
-// against 185 us for two waves of one CTA per SM.
-__global__ void __launch_bounds__(SMP_THREADS, 2) sampler_kernel(const SamplerParams p) {
+// MINB CTAs per SM.  Batches with more rows than SMs take the two-CTA build
+// (32 registers a thread, a few spilled), so that up to two rows per SM run as
+// one wave -- at B=256 165 us against 185 us for two waves; smaller batches
+// keep the one-CTA build (64 registers), whose greedy path is ~3 us faster.
+template <int MINB>
+__global__ void __launch_bounds__(SMP_THREADS, MINB) sampler_kernel(const SamplerParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SmpShared &sm = *reinterpret_cast<SmpShared *>(smem_raw);
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -525,8 +527,17 @@ __global__ void __launch_bounds__(SMP_THREADS, 2) sampler_kernel(const SamplerPa
 
 void launch_sampler(const SamplerParams &p, const LaunchCfg &lc, cudaError_t *e) {
     const size_t smem = sizeof(SmpShared);
+    int dev = 0, nsm = 0;
+    cudaError_t r0 = cudaGetDevice(&dev);
+    if (r0 == cudaSuccess) r0 = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (r0 != cudaSuccess) {
+        *e = r0;
+        return;
+    }
+    const bool two = p.B > nsm;
+    const void *kfn = two ? (const void *)sampler_kernel<2> : (const void *)sampler_kernel<1>;
     {
-        cudaError_t r = ensure_smem_attr((const void *)sampler_kernel, (int)smem);
+        cudaError_t r = ensure_smem_attr(kfn, (int)smem);
         if (r != cudaSuccess) {
             *e = r;
             return;
@@ -542,7 +553,7 @@ void launch_sampler(const SamplerParams &p, const LaunchCfg &lc, cudaError_t *e)
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = lc.pdl ? 1 : 0;
-    cudaError_t r = cudaLaunchKernelEx(&cfg, sampler_kernel, p);
+    cudaError_t r = two ? cudaLaunchKernelEx(&cfg, sampler_kernel<2>, p) : cudaLaunchKernelEx(&cfg, sampler_kernel<1>, p);
     if (r != cudaSuccess) *e = r;
 }
 
@@ -600,8 +611,11 @@ int static_setup(float **lpen, const char **err_msg) {
         if (e != cudaSuccess || !p)
             return static_fail(err_msg, RWKV7_ECUDA, "cudaGetSymbolAddress of the sampler scratch failed (error %lld)",
                                (long long)e);
-        e = cudaFuncSetAttribute(rk::sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(rk::sampler_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(rk::SmpShared));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(rk::sampler_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sizeof(rk::SmpShared));
         if (e != cudaSuccess)
             return static_fail(err_msg, RWKV7_ECUDA, "setting the sampler's shared-memory limit failed (error %lld)",
                                (long long)e);
