@@ -35,10 +35,10 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, workload, bytes)
 NCU_TRAFFIC = {
     ("gemm_tc_kernel", "2.9b"): (("recurrent_decode_gb300/csrc/gemm.cu", "recurrent_decode_gb300/csrc/gemm_common.cuh"),
-                                  "4a26b728954c9d79",
-                                  "2.9B shape, B=64: DRAM read+write of the 11 GEMM launches of one step of "
-                                  "a 2-layer cut (profiles/gemm_traffic_2.9b_b64.md), scaled to 32 layers + head, "
-                                  "per launch", 35823045),
+                                  "34251c189179fcd2",
+                                  "2.9B shape, B=64: DRAM read+write of the 9 GEMM launches of one step of "
+                                  "a 2-layer cut (ncu), scaled to 32 layers + head, "
+                                  "per launch", 44404130),
 }
 
 
