@@ -168,9 +168,13 @@ __global__ void embed_kernel(const ElemParams p) {
 // xl = LN(x[b]); for each mix q: xo[q][b] = fp16(xl + (shift - xl) * mu_q); shift <- xl.
 // NMIX = 6 for the time mix (r, w, k, v, a, g), 1 for the channel mix.  The
 // constants and the shift state (written only by this kernel, one step
-// earlier) are fetched before the dependency wait.
+// earlier) are fetched before the dependency wait.  Rows of up to 512 threads
+// (d <= 4096); bounded at that size the compiler takes up to 128 registers and
+// keeps more loads in flight (2.9B: 3.55 us a launch against 4.40 unbounded).
+// A two-rows-per-SM build for wide batches (64 registers, spills) measured
+// slower at 7.2B, B=256 (10.2 us against 8.8).
 template <int NMIX>
-__global__ void ln_mix_kernel(const ElemParams p) {
+__global__ void __launch_bounds__(512, 1) ln_mix_kernel(const ElemParams p) {
     __shared__ float red[64];
     if (threadIdx.x == 0) tl_start(p.tl);
     const int b = blockIdx.x;
@@ -302,6 +306,7 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
     if (tid < HS) {
         const int c = h * HS + tid;
         float kv = 0.f, vv = 0.f;
+#pragma unroll 4
         for (int j = 0; j < p.nsplit; ++j) {  // add the projection's k-split slabs in order
             const size_t o = (size_t)j * p.split_stride + off + tid;
             rv += p.r[o];
@@ -589,27 +594,33 @@ __global__ void __launch_bounds__(64) wkv_gate_kernel(const WkvSeqParams p) {
     p.z[off] = __float2half_rn((yn + p.bonus[(size_t)t * p.H + h] * vpv) * p.g[off]);
 }
 
-// LoRA-down outputs: one CTA per slot row; column c of LoRA i is the sum of the
-// S partial slabs, passed through the LoRA's activation and rounded to fp16.
+// LoRA-down outputs: one CTA per (slot row b, LoRA i); column c of LoRA i is
+// the sum of the S partial slabs, passed through the LoRA's activation and
+// rounded to fp16.  The LoRA's parameters are picked by constant index (an
+// array indexed by a register would be copied to local memory).
 __global__ void lora_fin_kernel(const LoraFinParams p) {
-    const int b = blockIdx.x;
+    const int b = blockIdx.x, i = blockIdx.y;
     if (threadIdx.x == 0) tl_start(p.tl);
+    int r, act;
+    const float *part;
+    __half *out;
+    switch (i) {
+        case 0: r = p.r[0], act = p.act[0], part = p.part[0], out = p.out[0]; break;
+        case 1: r = p.r[1], act = p.act[1], part = p.part[1], out = p.out[1]; break;
+        case 2: r = p.r[2], act = p.act[2], part = p.part[2], out = p.out[2]; break;
+        default: r = p.r[3], act = p.act[3], part = p.part[3], out = p.out[3]; break;
+    }
     pdl_wait();
     pdl_launch();
     if (threadIdx.x == 0) tl_release(p.tl);
-    const int total = p.r[0] + p.r[1] + p.r[2] + p.r[3];
-    for (int c = threadIdx.x; c < total; c += blockDim.x) {
-        int i = 0, col = c;
-        while (col >= p.r[i]) {
-            col -= p.r[i];
-            ++i;
-        }
-        const float *src = p.part[i] + (size_t)b * p.r[i] + col;
-        const long long stride = (long long)p.bcap * p.r[i];
+    const long long stride = (long long)p.bcap * r;
+    for (int col = threadIdx.x; col < r; col += blockDim.x) {
+        const float *src = part + (size_t)b * r + col;
         float acc = 0.0f;
-        for (int j = 0; j < p.S; ++j) acc += src[(size_t)j * stride];
-        const float y = p.act[i] == 1 ? fast_tanh(acc) : (p.act[i] == 2 ? fast_sigmoid(acc) : acc);
-        p.out[i][(size_t)b * p.r[i] + col] = __float2half_rn(y);
+#pragma unroll 4
+        for (int j = 0; j < p.S; ++j) acc += src[(size_t)j * stride];  // the k-split slabs in order
+        const float y = act == 1 ? fast_tanh(acc) : (act == 2 ? fast_sigmoid(acc) : acc);
+        out[(size_t)b * r + col] = __float2half_rn(y);
     }
     if (threadIdx.x == 0) tl_end(p.tl);
 }
@@ -750,7 +761,7 @@ void launch_wkv(const WkvParams &p, const LaunchCfg &lc, cudaError_t *e) {
 
 void launch_lora_fin(const LoraFinParams &p, const LaunchCfg &lc, cudaError_t *e) {
     cudaLaunchAttribute at[1];
-    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B), dim3(256), 0, lc, at);
+    cudaLaunchConfig_t cfg = mkcfg(dim3(p.B, 4), dim3(128), 0, lc, at);
     cudaError_t r = cudaLaunchKernelEx(&cfg, lora_fin_kernel, p);
     if (r != cudaSuccess) *e = r;
 }
