@@ -30,8 +30,12 @@
 using namespace rk;
 
 cudaError_t rk::ensure_smem_attr(const void *kernel, int bytes) {
-    // a fixed table (no heap allocation, so the allocation-free sampler path can
-    // use it); when it is full the attribute is simply set again on every call
+    // The kernel's dynamic shared-memory limit on the current device is raised
+    // to the largest size asked for so far and never lowered (a launch of a
+    // smaller size fits under it; lowering it would break a later, larger
+    // launch that the table already counts as set).  A fixed table (no heap
+    // allocation, so the allocation-free sampler path can use it); when it is
+    // full the attribute is simply set again on every call.
     struct Entry {
         const void *kernel;
         int dev, bytes;
@@ -43,11 +47,19 @@ cudaError_t rk::ensure_smem_attr(const void *kernel, int bytes) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(mu);
+    int at = -1;
     for (int i = 0; i < ndone; ++i)
-        if (done[i].kernel == kernel && done[i].dev == dev && done[i].bytes == bytes) return cudaSuccess;
+        if (done[i].kernel == kernel && done[i].dev == dev) {
+            if (done[i].bytes >= bytes) return cudaSuccess;
+            at = i;
+        }
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess && ndone < 256) done[ndone++] = Entry{kernel, dev, bytes};
-    return e;
+    if (e != cudaSuccess) return e;
+    if (at >= 0)
+        done[at].bytes = bytes;
+    else if (ndone < 256)
+        done[ndone++] = Entry{kernel, dev, bytes};
+    return cudaSuccess;
 }
 
 namespace {
