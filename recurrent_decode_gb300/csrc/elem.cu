@@ -318,6 +318,15 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
         mbar_expect_tx(&sm.full, HS * HS * 4);
         bulk_g2s(sm.st, S, HS * HS * 4, &sm.full);
     }
+    // the layer's per-channel constants, before the dependency wait (kept as
+    // fp16 pairs: the registers live across the state update)
+    const int c = h * HS + (tid & (HS - 1));
+    __half2 kkka = __float2half2_rn(0.f), rkg = kkka, lnwb = kkka;
+    if (tid < HS) {
+        kkka = __halves2half2(p.k_k[c], p.k_a[c]);
+        rkg = __halves2half2(p.r_k[c], p.r_k[c]);
+        lnwb = __halves2half2(p.lnx_w[c], p.lnx_b[c]);
+    }
     pdl_wait();
     pdl_launch();
     if (tid == 0) tl_release(p.tl);
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
     const size_t off = (size_t)b * p.d + (size_t)h * HS;
     float rv = 0.f, kpv = 0.f, vpv = 0.f;
     if (tid < HS) {
-        const int c = h * HS + tid;
+        // every vector of the pair requested at once, then used
         float kv = 0.f, vv = 0.f;
 #pragma unroll 4
         for (int j = 0; j < p.nsplit; ++j) {  // add the projection's k-split slabs in order
@@ -335,20 +344,22 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
             vv += p.v[o];
         }
         const float av = p.a[off + tid];
-        const float kk = kv * __half2float(p.k_k[c]);
+        const float decv = p.dec[off + tid];
+        const float vf = p.layer == 0 ? 0.f : p.v_first[off + tid];
+        const float vgv = p.layer == 0 ? 0.f : p.vg[off + tid];
+        const float kk = kv * __low2float(kkka);
         const float ss = sum64(kk * kk, sm.red, 1);
         const float khv = kk / fmaxf(sqrtf(ss), 1e-12f);
-        kpv = kv * (1.0f + (av - 1.0f) * __half2float(p.k_a[c]));
+        kpv = kv * (1.0f + (av - 1.0f) * __high2float(kkka));
         if (p.layer == 0) {
             vpv = vv;
             p.v_first[off + tid] = vv;
         } else {
-            const float vf = p.v_first[off + tid];
-            vpv = vv + (vf - vv) * p.vg[off + tid];
+            vpv = vv + (vf - vv) * vgv;
         }
         sm.kh[tid] = khv;
         sm.ka[tid] = khv * av;
-        sm.dec[tid] = p.dec[off + tid];
+        sm.dec[tid] = decv;
         sm.kp[tid] = kpv;
         sm.vp[tid] = vpv;
         sm.r[tid] = rv;
@@ -391,11 +402,10 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
     }
     __syncthreads();
     if (tid < HS) {
-        const int c = h * HS + tid;
         const float yv = sm.y[tid];
         // the GroupNorm moments and the bonus sum of the head in one reduction
         Moments m{1.0f, yv, 0.0f};
-        float bz = rv * kpv * __half2float(p.r_k[c]);
+        float bz = rv * kpv * __low2float(rkg);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const Moments x{__shfl_xor_sync(0xffffffffu, m.n, o), __shfl_xor_sync(0xffffffffu, m.s, o),
@@ -416,7 +426,7 @@ __global__ void __launch_bounds__(WKV_THREADS, 12) wkv_kernel(const WkvParams p)
         const float mean = t.s * (1.0f / HS);
         const float dv = yv - mean;
         const float var = t.m2 * (1.0f / HS);
-        const float yn = dv * (1.0f / sqrtf(var + 64e-5f)) * __half2float(p.lnx_w[c]) + __half2float(p.lnx_b[c]);
+        const float yn = dv * (1.0f / sqrtf(var + 64e-5f)) * __low2float(lnwb) + __high2float(lnwb);
         p.z[off + tid] = __float2half_rn((yn + bonus * vpv) * p.g[off + tid]);
         if (tid == 0) tl_end(p.tl);
     }
