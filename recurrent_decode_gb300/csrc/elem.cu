@@ -213,8 +213,10 @@ __global__ void __launch_bounds__(512, 1) ln_mix_kernel(const ElemParams p) {
         for (int q = 0; q < NMIX; ++q) mu4[q] = *reinterpret_cast<const uint4 *>(p.mu[q] + i0);
         if (ok) ld8f(shp, sh);
     }
-    pdl_wait();
+    // Dependents may launch as soon as every row has started: the GEMM that
+    // follows then fetches its first weight stages while this kernel waits.
     pdl_launch();
+    pdl_wait();
     if (threadIdx.x == 0) tl_release(p.tl);
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (act) {
@@ -660,8 +662,8 @@ __global__ void lora_fin_kernel(const LoraFinParams p) {
         case 2: r = p.r[2], act = p.act[2], part = p.part[2], out = p.out[2]; break;
         default: r = p.r[3], act = p.act[3], part = p.part[3], out = p.out[3]; break;
     }
+    pdl_launch();  // as in ln_mix_kernel: the LoRA-up GEMM may launch and prefetch now
     pdl_wait();
-    pdl_launch();
     if (threadIdx.x == 0) tl_release(p.tl);
     const long long stride = (long long)p.bcap * r;
     for (int col = threadIdx.x; col < r; col += blockDim.x) {
