@@ -252,8 +252,8 @@ __global__ void ln_out_kernel(const ElemParams p) {
         w4 = *reinterpret_cast<const uint4 *>(p.ln_w + i0);
         b4 = *reinterpret_cast<const uint4 *>(p.ln_b + i0);
     }
+    pdl_launch();  // the head GEMM may launch and prefetch while this waits
     pdl_wait();
-    pdl_launch();
     if (threadIdx.x == 0) tl_release(p.tl);
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (act) {
