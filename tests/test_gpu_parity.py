@@ -398,6 +398,39 @@ def test_sampler_bit_exact_against_oracle():
             assert got[s] == tok, (rnd, s, got[s], tok)
 
 
+def test_sampler_wide_batch_bit_exact_against_oracle():
+    """A batch with more rows than SMs takes the sampler's two-CTAs-per-SM build:
+    its tokens equal the oracle sampler's, row for row, over a few rounds."""
+    torch = _torch()
+    import recurrent_decode_gb300 as rd
+    dev = torch.device("cuda")
+    dims = synth.Dims("0.1b")
+    B = torch.cuda.get_device_properties(0).multi_processor_count + 8
+    ctx = rd.Rwkv7(dims, B)
+    occ, full = [], []
+    for s in range(B):
+        f = dict(temperature=1.0, top_p=1.0, top_k=0, presence=0.0, frequency=0.0, penalty_decay=1.0,
+                 greedy=False, seed=3000 + s)
+        f.update(SAMPLER_CASES[s % len(SAMPLER_CASES)])
+        full.append(f)
+        ctx.set_sampling(s, **f)
+        occ.append(np.zeros(dims.vocab, np.float32))
+    slots = torch.arange(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    draws = [0] * B
+    for rnd in range(4):
+        lg = synth.random_logits(B, dims.vocab, seed=900 + rnd, scale=1.0 + rnd)
+        ctx.sample_batch(slots, torch.from_numpy(lg).to(dev), nxt)
+        ctx.synchronize()
+        got = nxt.cpu().numpy()
+        for s, p in enumerate(full):
+            tok, _ = oracle.sample(lg[s], occ[s], p, draws[s])
+            if not p["greedy"]:
+                draws[s] += 1
+            assert got[s] == tok, (rnd, s, got[s], tok)
+    ctx.close()
+
+
 def test_device_side_argument_errors_are_reported(tiny):
     torch = _torch()
     import recurrent_decode_gb300 as rd
