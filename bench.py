@@ -666,8 +666,13 @@ def main():
 
     def family(times):
         gemm_cls = [k for k in times if k.startswith("gemm") and k in cb]
+        # the r, k, v launch carries the LoRA up projections too when they are
+        # fused into it (no gemm_lora launches in the step)
+        cbx = dict(cb)
+        if "gemm_proj" in times and "gemm_lora" not in times:
+            cbx["gemm_proj"] = cb["gemm_proj"] + cb["gemm_lora"]
         return {"gemm_tc_kernel": (sum(times[k][0] for k in gemm_cls), sum(times[k][1] for k in gemm_cls),
-                                   sum(cb[k] for k in gemm_cls)),
+                                   sum(cbx[k] for k in gemm_cls)),
                 "wkv_kernel": (times["wkv"][0], times["wkv"][1], cb["wkv"])}
 
     kern = family(ig)

@@ -27,7 +27,8 @@ namespace rk {
 
 // The items of CTA c: its phase-0 items (two-phase launches: items [0, n0)
 // spread over CTAs [0, g0)), then its phase-1 items (items [n0, nitems) spread
-// over every CTA).  A single-phase launch has n0 = 0.
+// over CTAs [0, p1a) and [p1b, G), numbered in that order).  A single-phase
+// launch has n0 = 0.
 struct ItemSpan {
     int a0, a1, b0, b1;
     __device__ __forceinline__ void init(const GemmParams &p, int c, int G) {
@@ -37,8 +38,13 @@ struct ItemSpan {
             a0 = item_first(c, p.g0, n0);
             a1 = item_first(c + 1, p.g0, n0);
         }
-        b0 = n0 + item_first(c, G, n1);
-        b1 = n0 + item_first(c + 1, G, n1);
+        b0 = b1 = n0;
+        const int v = c < p.p1a ? c : (c >= p.p1b ? c - p.p1b + p.p1a : -1);
+        const int G1 = p.p1a + G - p.p1b;
+        if (v >= 0) {
+            b0 = n0 + item_first(v, G1, n1);
+            b1 = n0 + item_first(v + 1, G1, n1);
+        }
     }
     __device__ __forceinline__ int count() const { return (a1 - a0) + (b1 - b0); }
     __device__ __forceinline__ int at(int k) const { return k < a1 - a0 ? a0 + k : b0 + (k - (a1 - a0)); }
@@ -76,9 +82,10 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
     __shared__ GemmSeg sseg[GEMM_MAX_SEG];
     __shared__ uint32_t snz[MAX_NZ_BLOCKS];
     __shared__ uint64_t flags_ready;
-    __shared__ uint32_t s_ok;
+    __shared__ uint32_t s_ok, s_last;
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int S = p.stages, B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, n0 = p.n0;
+    const int S = p.stages, B = p.B, npad = p.npad, NB = p.accbufs, nseg = p.nseg, n0 = p.n0, ndep = p.ndep;
+    const uint32_t dep_target = (uint32_t)p.dep_target;
     const bool has_skip = p.nz_skip != nullptr;
     const uint32_t *skip = has_skip ? snz : nullptr;
     const uint32_t XKB = (uint32_t)npad * 128u;  // one activation k-block
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             pdl_launch();
             tl_release(p.tl);
             bool ok = true;
-            bool dep_ok = n0 == 0, flags_ok = !has_skip;
+            bool dep_ok = dep_target == 0u, flags_ok = !has_skip;
             // phase-1 stages whose weights are requested but whose activations
             // wait for phase 0 (at most S of them: the ring)
             int pend_kb[8], pend_s[8], pend_st[8], npend = 0;
@@ -185,7 +192,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             // wait for phase 0, then release the pending activation copies
             auto resolve = [&]() -> bool {
                 if (!dep_ok) {
-                    if (!wait_count(p.dep, (uint32_t)n0, abort_flag)) return false;
+                    if (!wait_count(p.dep, dep_target, abort_flag)) return false;
                     fence_proxy_async_global();  // phase 0 wrote them through the generic proxy
                     dep_ok = true;
                 }
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
                         mbar_expect_tx(&full[st], W_STAGE_BYTES + XB);
                         tma_load_3d(sW + (size_t)st * W_STAGE_BYTES, wm, &full[st], 0, 0, tb + kb, polW);
                     }  // else: the weights were requested before the dependency wait
-                    if (ph1 && !dep_ok && check_count(p.dep, (uint32_t)n0)) {
+                    if (ph1 && !dep_ok && check_count(p.dep, dep_target)) {
                         fence_proxy_async_global();
                         dep_ok = true;
                     }
@@ -335,8 +342,8 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
             const int i = span.at(k);
             const bool ph1 = i >= n0;
             if (ph1 && !ph1_ready) {
-                if (n0 > 0) {  // wait for every phase-0 item (all CTAs) to be stored
-                    if (et == 0) s_ok = wait_count(p.dep, (uint32_t)n0, abort_flag) ? 1u : 0u;
+                if (dep_target > 0u) {  // wait for the phase-0 items that feed phase 1 (all CTAs) to be stored
+                    if (et == 0) s_ok = wait_count(p.dep, dep_target, abort_flag) ? 1u : 0u;
                     named_bar(3, EPI_THREADS);
                     const bool ok_dep = s_ok != 0u;
                     named_bar(3, EPI_THREADS);
@@ -401,9 +408,27 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1) gemm_tc_kernel(const __gri
                 }
                 named_bar(2, EPI_THREADS);
             }
-            if (!ph1) {  // a phase-0 item is stored: count it (release)
+            if (i < ndep) {  // a phase-0 item that feeds phase 1 is stored: count it (release)
                 named_bar(3, EPI_THREADS);
-                if (et == 0) {
+                if (sg.S > 1 && sg.fix_out != nullptr) {
+                    // split: the tile's last item to arrive adds the slabs and
+                    // finishes the tile, then counts it
+                    if (et == 0) {
+                        __threadfence();
+                        const uint32_t prev = atomicAdd(sg.fix_ctr + it.tile, 1u);
+                        s_last = prev == (uint32_t)(sg.S - 1) ? 1u : 0u;
+                        __threadfence();
+                    }
+                    named_bar(3, EPI_THREADS);
+                    if (s_last != 0u) {
+                        fix_item(sseg[it.s], nrow, npad, B, grp * EPI_CW);
+                        named_bar(3, EPI_THREADS);
+                        if (et == 0) {
+                            __threadfence();
+                            atomicAdd(p.dep, 1u);
+                        }
+                    }
+                } else if (et == 0) {
                     __threadfence();
                     atomicAdd(p.dep, 1u);
                 }

@@ -154,6 +154,49 @@ static __device__ __noinline__ bool epi_item(const GemmSeg &sg, uint32_t taddr, 
         default: return false;
     }
 }
+// Finish row n of a split tile (GemmSeg::fix_out): add the S partial slabs in
+// slab order, apply the fp16 kind fix_epi, store.  The slabs were written by
+// other SMs: read through L2, the loads of up to FIX_BATCH slabs in flight at
+// once (an L2 round trip under the weight stream costs about a microsecond).
+// Columns as in epi_run.
+constexpr int FIX_BATCH = 4;
+__device__ __forceinline__ void fix_item(const GemmSeg &sg, int n, int npad, int B, int c0) {
+    if (n >= sg.rows) return;
+    constexpr int HW = EPI_CW / 2;  // columns per pass
+    const int kind = sg.fix_epi;
+    const float *src = (const float *)sg.out + n;
+    __half *dst = (__half *)sg.fix_out + n;
+    for (int cb = c0; cb < npad; cb += EPI_GROUPS * EPI_CW) {
+        for (int h = cb; h < cb + EPI_CW; h += HW) {
+            const int nq = min(HW, B - h);
+            if (nq <= 0) break;
+            float v[HW];
+            for (int j0 = 0; j0 < sg.S; j0 += FIX_BATCH) {
+                float t[FIX_BATCH][HW];
+#pragma unroll
+                for (int j = 0; j < FIX_BATCH; ++j) {
+                    const float *sj = src + (size_t)(j0 + j) * sg.split_stride + (size_t)h * sg.ldo;
+#pragma unroll
+                    for (int q = 0; q < HW; ++q)
+                        t[j][q] = (j0 + j < sg.S && q < nq) ? __ldcg(sj + (size_t)q * sg.ldo) : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < FIX_BATCH; ++j)
+#pragma unroll
+                    for (int q = 0; q < HW; ++q)
+                        if (j0 + j < sg.S) v[q] = (j0 + j == 0) ? t[j][q] : v[q] + t[j][q];
+            }
+#pragma unroll
+            for (int q = 0; q < HW; ++q) {
+                float y = v[q];
+                if (kind == EPI_F16_TANH) y = fast_tanh(y);
+                else if (kind == EPI_F16_SIGMOID) y = fast_sigmoid(y);
+                if (q < nq) dst[(size_t)(h + q) * sg.ldo] = __float2half_rn(y);
+            }
+        }
+    }
+}
+
 // The bias an epilogue of weight row n needs (0 for kinds without one).
 __device__ __forceinline__ float epi_bias(const GemmSeg &sg, int n) {
     return (sg.S == 1 && (sg.epi == EPI_DECAY || sg.epi == EPI_SIGMOID_BIAS) && n < sg.rows) ? __half2float(sg.bias[n])

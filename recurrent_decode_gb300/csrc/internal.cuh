@@ -24,8 +24,8 @@ constexpr int HS = 64;             // head size
 constexpr int MAX_B = 256;         // slots per fused step
 constexpr int GEMM_TILE_M = 128;   // weight rows per tile (MMA M)
 constexpr int GEMM_TILE_K = 64;    // reduction elements per stage (128 bytes of fp16)
-constexpr int GEMM_MAX_SEG = 8;
-constexpr int GEMM_MAX_MAPS = 16;
+constexpr int GEMM_MAX_SEG = 12;
+constexpr int GEMM_MAX_MAPS = 24;
 constexpr int MAX_SPLIT = 16;         // k-splits of one projection
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bounded waits give up after ~2 s
 
@@ -64,6 +64,14 @@ struct GemmSeg {
     const __half *w;      // tiled weights of this layer (SIMT path)
     const __half *x;      // activations [B][ldx] (SIMT path)
     int ldx;
+    // Split segment finished in the launch (two-phase launches): each row
+    // tile's last item to store its partial slab adds the S slabs in slab
+    // order, applies fix_epi (an fp16 kind) and stores the result at fix_out
+    // (element b * ldo + n).  fix_ctr: one counter per row tile, zero at
+    // launch.  Null fix_out: the consumer adds the slabs.
+    void *fix_out;
+    uint32_t *fix_ctr;
+    int fix_epi;
 };
 
 struct GemmParams {
@@ -83,11 +91,15 @@ struct GemmParams {
     uint32_t *err;
     unsigned long long *tl;          // timeline words of this launch (measurement only; else null)
     // Two-phase launch: items [0, n0) (the first segments) are phase 0, spread
-    // over CTAs [0, g0); the rest are phase 1, spread over every CTA, and their
-    // activations -- produced by phase 0 -- are read only once *dep (zero at
-    // launch, counted up per stored phase-0 item) reaches n0.  Every CTA must be
-    // resident at once: the grid is at most one CTA per SM.  n0 = 0: one phase.
-    int n0, g0;
+    // over CTAs [0, g0); the rest are phase 1, spread over CTAs [0, p1a) and
+    // [p1b, grid), and their activations -- produced by the phase-0 items
+    // [0, ndep) -- are read only once *dep (zero at launch) reaches dep_target:
+    // each stored unsplit item of [0, ndep) adds one, each row tile of a split
+    // segment finished in the launch (GemmSeg::fix_out) one.  Phase-0 items
+    // past ndep feed no phase-1 item and run beside the chain.  Every CTA must
+    // be resident at once: the grid is at most one CTA per SM.  n0 = 0: one
+    // phase (p1a = p1b = 0).
+    int n0, g0, ndep, dep_target, p1a, p1b;
     uint32_t *dep;
     int skip_seg;                    // segment whose activations nz_skip describes
 };

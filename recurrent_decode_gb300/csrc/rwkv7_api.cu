@@ -162,7 +162,10 @@ struct rwkv7_ctx {
     float *pr = nullptr, *pk = nullptr, *pv = nullptr, *phw = nullptr, *pha = nullptr, *phv = nullptr,
           *phg = nullptr, *px = nullptr;
     uint32_t *errw = nullptr;
-    uint32_t *ffn_dep = nullptr;  // per layer: key-projection items stored (fused channel mix), zeroed per step
+    // per layer: key-projection items stored (fused channel mix); per layer:
+    // LoRA-down tiles finished (fused r, k, v + LoRA launch); per layer
+    // FIX_TILES_PER_LAYER split-tile counters of that launch; zeroed per step
+    uint32_t *ffn_dep = nullptr;
     unsigned long long *nzstat = nullptr;  // nonzero channel-mix blocks counted by the key projection
     unsigned long long nz_considered = 0;  // blocks those counts cover (host side)
     // prefill: second residual buffer and WKV work buffers [bcap][d] ([bcap][H] bonus)
@@ -302,6 +305,24 @@ int split_for(const rwkv7_ctx *c, int tiles, int pairs) {
     return std::max(1, std::min(s, std::min(MAX_SPLIT, pairs)));
 }
 
+// Split-tile counters per layer of the fused r, k, v + LoRA launch (LoRA-down
+// row tiles of all four LoRAs).
+constexpr int FIX_TILES_PER_LAYER = 16;
+
+// Split factor of the LoRA-down items in the fused r, k, v + LoRA launch.
+// Unsplit when a LoRA-down tile is no longer than an r, k, v item (s1
+// splits); otherwise split to about half an r, k, v item, so that the LoRA
+// chain (down, finish, up) ends while r, k, v still stream -- the finish costs
+// a few L2 round trips, which pay only against a long chain.  Depends only on
+// the shapes.  RWKV7_LORA_SPLIT overrides it (tuning knob).
+int lora_split(const rwkv7_ctx *c, int s1) {
+    const int pairs = kblocks(c, L_W1) / 2;
+    const int item = std::max(1, kblocks(c, L_WR) / 2 / std::max(1, s1));
+    int sd = pairs <= item ? 1 : (2 * pairs + item - 1) / item;
+    sd = env_int("RWKV7_LORA_SPLIT", sd);
+    return std::max(1, std::min(sd, std::min(MAX_SPLIT, pairs)));
+}
+
 // Split factors of the step's split-K projections: r, k, v + LoRA-down (s1),
 // output (s3) and channel-mix value (s5).
 void step_splits(const rwkv7_ctx *c, int *s1, int *s3, int *s5) {
@@ -360,6 +381,8 @@ struct Seg {
     int ldo;
     const __half *bias;
     int S;        // k-splits (S > 1: raw fp32 partials, slab stride bcap * ldo)
+    void *fix_out = nullptr;  // S > 1 in a two-phase launch: the tile's last split finishes it here
+    int fix_epi = 0;          // with this fp16 kind
 };
 
 // The channel mix runs as one two-phase launch (key projection, then the value
@@ -369,12 +392,28 @@ bool ffn_fused(const rwkv7_ctx *c, int mode) {
     return c->wbits == 16 && (mode == 0 || mode == 1) && env_int("RWKV7_FUSE_FFN", 1) != 0;  // tuning knob
 }
 
+// The r, k, v projections, the LoRA down projections and the LoRA up
+// projections with their gates run as one two-phase launch: the LoRA-down
+// items (unsplit, their epilogues write the activated fp16 hidden) are phase 0
+// and counted; the r, k, v items run beside them; the LoRA-up items are phase
+// 1 and read the hidden once every LoRA-down item is stored.  The LoRA chain
+// then overlaps the r, k, v weight stream instead of following it as two more
+// launches.  fp16 tensor-core modes only; otherwise three launches.
+bool att_fused(const rwkv7_ctx *c, int mode) {
+    return c->wbits == 16 && (mode == 0 || mode == 1) && env_int("RWKV7_FUSE_ATT", 1) != 0;  // tuning knob
+}
+
 // nseg0 > 0: a two-phase launch whose first nseg0 segments are phase 0 and
-// whose phase-1 activations wait for them through the counter *dep (fp16
-// tensor-core kernel only).
+// whose phase-1 activations wait, through the counter *dep, for the items of
+// the first nsegdep of them (all nseg0 when nsegdep < 0); fp16 tensor-core
+// kernel only.  full_grid: one CTA on every SM (else as many as the larger
+// phase has items).
 int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *nz_out, const uint32_t *nz_skip,
              const LaunchCfg &lc, int mode, unsigned long long *tl = nullptr, int nseg0 = 0,
-             uint32_t *dep = nullptr) {
+             uint32_t *dep = nullptr, int nsegdep = -1, bool full_grid = false, uint32_t *tile_ctr = nullptr) {
+    if (nsegdep < 0 || nsegdep > nseg0) nsegdep = nseg0;
+    int nfix_tiles = 0;   // tile counters handed out so far
+    bool split_dep = false;
     GemmParams p;
     memset(&p, 0, sizeof p);
     p.tl = tl;
@@ -437,7 +476,18 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
             g.item0 = item;
             item += g.tiles * g.S;
         }
+        if (sg.fix_out != nullptr) {  // a split finished in the launch (counted per tile)
+            if (s >= nsegdep || g.S < 2 || !tile_ctr || nfix_tiles + g.tiles > FIX_TILES_PER_LAYER)
+                return fail(c, RWKV7_ECUDA, "internal: bad split fix-up segment");
+            g.fix_out = sg.fix_out;
+            g.fix_epi = sg.fix_epi;
+            g.fix_ctr = tile_ctr + nfix_tiles;
+            nfix_tiles += g.tiles;
+            split_dep = true;
+        }
+        if (s < nsegdep) p.dep_target += g.fix_out ? g.tiles : g.tiles * g.S;
         if (s + 1 == nseg0) p.n0 = item;  // phase-0 items: those of the first nseg0 segments
+        if (s + 1 == nsegdep) p.ndep = item;  // of which those that feed phase 1
     }
     p.nseg = n;
     p.nmaps = nmaps;
@@ -496,7 +546,35 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
             if (!dep || mode == 2 || w8) return fail(c, RWKV7_ECUDA, "internal: two-phase launch");
             p.dep = dep;
             p.g0 = std::min(p.n0, c->nsm);
-            grid = std::min(c->nsm, std::max(p.g0, p.nitems - p.n0));
+            grid = full_grid ? c->nsm : std::min(c->nsm, std::max(p.g0, p.nitems - p.n0));
+            // Phase-1 CTAs.  Where only some phase-0 items feed phase 1 (the
+            // chain), phase 1 goes where it starts soonest.  The predecessor
+            // (one LayerNorm row per CTA, a whole SM each) holds B SMs when
+            // this launch begins, and the CTAs placed there start late, so
+            // with split (short) chain items phase 1 runs on the first
+            // nsm - B CTAs: the chain's and the early r, k, v ones.  Without
+            // such room (B near nsm or more), on the chain's CTAs and the idle
+            // ones; with unsplit (long) chain items, on every CTA but the
+            // chain's.
+            p.p1a = p.p1b = 0;
+            if (p.ndep < p.n0) {
+                int gdep = 0;  // CTAs holding items of [0, ndep)
+                while (gdep < p.g0 && (long long)gdep * p.n0 / p.g0 < p.ndep) ++gdep;
+                const int early = c->nsm - B;
+                const int n1 = p.nitems - p.n0;
+                int pm = !split_dep ? 0 : (early >= gdep + 1 && early >= n1 / 2) ? 3 : 1;
+                pm = env_int("RWKV7_PHASE1_CTAS", pm);  // tuning knob
+                if (pm == 3) {
+                    p.p1a = std::min(early, grid);
+                    p.p1b = grid;
+                } else if (pm == 1) {
+                    p.p1a = gdep;
+                    p.p1b = p.g0;
+                } else if (pm == 0) {
+                    p.p1b = gdep;
+                }
+            }
+            if (p.p1a + grid - p.p1b < 1) return fail(c, RWKV7_ECUDA, "internal: two-phase launch without phase-1 CTAs");
             p.accbufs = (2 * p.npad <= 512) ? 2 : 1;
         }
         launch_gemm_tc(p, grid, gemm_tc_smem_bytes(p.npad, stages), lc, &e);
@@ -556,9 +634,9 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     ep.emb = c->w[W_EMB];
     ep.ln_w = c->w[W_LN0W];
     ep.ln_b = c->w[W_LN0B];
-    const bool fuse_ffn = ffn_fused(c, mode);
-    if (fuse_ffn) {  // the per-layer counters of the fused channel mix start at zero every step
-        e = cudaMemsetAsync(c->ffn_dep, 0, (size_t)c->L * 4, st);
+    const bool fuse_ffn = ffn_fused(c, mode), fuse_att = att_fused(c, mode);
+    if (fuse_ffn || fuse_att) {  // the per-layer counters of the two-phase launches start at zero every step
+        e = cudaMemsetAsync(c->ffn_dep, 0, (2 + FIX_TILES_PER_LAYER) * (size_t)c->L * 4, st);
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "counter reset: %s", cudaGetErrorString(e));
     }
     pb(P_EMBED);
@@ -570,6 +648,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     int rc;
     int s1, s3, s5;  // depend only on the shapes, so a slot's result does not depend on B
     step_splits(c, &s1, &s3, &s5);
+    const int sd = lora_split(c, s1);
     const long long xstride = (long long)c->bcap * d;
     int px_splits = 0;  // residual partial slabs in c->px still to be added to x
     for (int l = 0; l < c->L; ++l) {
@@ -592,6 +671,42 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         launch_ln_mix(m, 6, lc, &e);
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "ln_mix launch: %s", cudaGetErrorString(e));
+        // LoRA up projections with their gates (G2)
+        Seg g2[4];
+        int n2 = 0;
+        g2[n2++] = {L_W2, A_HW, c->hw, c->rw, EPI_DECAY, c->dec, d, LW(c, L_W0, l), 1};
+        g2[n2++] = {L_A2, A_HA, c->ha, c->ra, EPI_SIGMOID_BIAS, c->a, d, LW(c, L_A0, l), 1};
+        if (l > 0) g2[n2++] = {L_V2, A_HV, c->hv, c->rv, EPI_SIGMOID_BIAS, c->vg, d, LW(c, L_V0, l), 1};
+        g2[n2++] = {L_G2, A_HG, c->hg, c->rg, EPI_F32, c->g, d, nullptr, 1};
+        if (fuse_att) {
+            // One two-phase launch: LoRA down (unsplit, activated fp16 hidden;
+            // counted), r, k, v (s1 partial slabs, beside the chain), then the
+            // LoRA up projections (phase 1).
+            Seg ga[11];
+            int na = 0;
+            if (sd == 1) {
+                ga[na++] = {L_W1, A_XW, c->xmix[1], d, EPI_F16_TANH, c->hw, c->rw, nullptr, 1};
+                ga[na++] = {L_A1, A_XA, c->xmix[4], d, EPI_F16, c->ha, c->ra, nullptr, 1};
+                if (l > 0) ga[na++] = {L_V1, A_XV, c->xmix[3], d, EPI_F16, c->hv, c->rv, nullptr, 1};
+                ga[na++] = {L_G1, A_XG, c->xmix[5], d, EPI_F16_SIGMOID, c->hg, c->rg, nullptr, 1};
+            } else {  // sd partial slabs per tile, finished by the tile's last split
+                ga[na++] = {L_W1, A_XW, c->xmix[1], d, EPI_F32, c->phw, c->rw, nullptr, sd, c->hw, EPI_F16_TANH};
+                ga[na++] = {L_A1, A_XA, c->xmix[4], d, EPI_F32, c->pha, c->ra, nullptr, sd, c->ha, EPI_F16};
+                if (l > 0) ga[na++] = {L_V1, A_XV, c->xmix[3], d, EPI_F32, c->phv, c->rv, nullptr, sd, c->hv, EPI_F16};
+                ga[na++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, sd, c->hg, EPI_F16_SIGMOID};
+            }
+            const int ndown = na;
+            ga[na++] = {L_WR, A_XR, c->xmix[0], d, EPI_F32, c->pr, d, nullptr, s1};
+            ga[na++] = {L_WK, A_XK, c->xmix[2], d, EPI_F32, c->pk, d, nullptr, s1};
+            ga[na++] = {L_WV, A_XV, c->xmix[3], d, EPI_F32, c->pv, d, nullptr, s1};
+            const int nph0 = na;
+            for (int q = 0; q < n2; ++q) ga[na++] = g2[q];
+            pb(P_GEMM_PROJ);
+            if ((rc = run_gemm(c, l, ga, na, B, nullptr, nullptr, lc, mode, tlp(P_GEMM_PROJ), nph0,
+                               c->ffn_dep + c->L + l, ndown, true, c->ffn_dep + 2 * (size_t)c->L + (size_t)FIX_TILES_PER_LAYER * l)))
+                return rc;
+            pe();
+        } else {
         // G1: r, k, v and the LoRA down projections, as s1 partial slabs.  Without
         // a k-split the LoRA-down epilogues apply the activation and write the
         // fp16 hidden themselves (the LoRA finalize kernel would only convert).
@@ -632,16 +747,10 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         pe();
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "lora_fin launch: %s", cudaGetErrorString(e));
         }
-        // G2: LoRA up projections with their gates
-        Seg g2[4];
-        int n2 = 0;
-        g2[n2++] = {L_W2, A_HW, c->hw, c->rw, EPI_DECAY, c->dec, d, LW(c, L_W0, l), 1};
-        g2[n2++] = {L_A2, A_HA, c->ha, c->ra, EPI_SIGMOID_BIAS, c->a, d, LW(c, L_A0, l), 1};
-        if (l > 0) g2[n2++] = {L_V2, A_HV, c->hv, c->rv, EPI_SIGMOID_BIAS, c->vg, d, LW(c, L_V0, l), 1};
-        g2[n2++] = {L_G2, A_HG, c->hg, c->rg, EPI_F32, c->g, d, nullptr, 1};
         pb(P_GEMM_LORA);
         if ((rc = run_gemm(c, l, g2, n2, B, nullptr, nullptr, lc, mode, tlp(P_GEMM_LORA)))) return rc;
         pe();
+        }
         // WKV7 + GroupNorm + bonus + gate (adds the r, k, v slabs)
         WkvParams wp;
         memset(&wp, 0, sizeof wp);
@@ -1103,7 +1212,7 @@ int rwkv7_create_ex(const rwkv7_config *cfg, int32_t weight_bits, void *cuda_str
         (rc = dalloc(c, &c->phg, SR * c->rg)))
         return bad(rc);
     if ((rc = dalloc(c, &c->errw, 16))) return bad(rc);
-    if ((rc = dalloc(c, &c->ffn_dep, (size_t)L))) return bad(rc);
+    if ((rc = dalloc(c, &c->ffn_dep, (2 + FIX_TILES_PER_LAYER) * (size_t)L))) return bad(rc);
     if ((rc = dalloc(c, &c->nzstat, 4))) return bad(rc);
     if ((rc = dalloc(c, &c->x2, R * d)) || (rc = dalloc(c, &c->pf_vec, R * 6 * (size_t)d)) ||
         (rc = dalloc(c, &c->pf_y, R * d)) || (rc = dalloc(c, &c->pf_bonus, R * c->H)))
@@ -1498,8 +1607,8 @@ int32_t rwkv7_step_kernel_count(const rwkv7_ctx *c, int32_t B, int32_t with_samp
     int s1, s3, s5;
     step_splits(c, &s1, &s3, &s5);
     // the LoRA finalize kernel runs only for a split r, k, v GEMM; the fused
-    // channel mix is one launch
-    const int per_layer = (s1 == 1 ? 8 : 9) - (ffn_fused(c, c->mode) ? 1 : 0);
+    // channel mix is one launch; the fused r, k, v + LoRA launch replaces three
+    const int per_layer = (att_fused(c, c->mode) ? 6 : (s1 == 1 ? 7 : 8)) + (ffn_fused(c, c->mode) ? 0 : 1);
     return sub * (1 + per_layer * c->L + 2 + (with_sampling ? 1 : 0));
 }
 
