@@ -35,10 +35,10 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, workload, bytes)
 NCU_TRAFFIC = {
     ("gemm_tc_kernel", "2.9b"): (("recurrent_decode_gb300/csrc/gemm.cu", "recurrent_decode_gb300/csrc/gemm_common.cuh"),
-                                  "34251c189179fcd2",
-                                  "2.9B shape, B=64: DRAM read+write of the 9 GEMM launches of one step of "
+                                  "954915d205220eda",
+                                  "2.9B shape, B=64: DRAM read+write of the 7 GEMM launches of one step of "
                                   "a 2-layer cut (ncu), scaled to 32 layers + head, "
-                                  "per launch", 44404130),
+                                  "per launch", 59051560),
 }
 
 

@@ -155,7 +155,8 @@ static __device__ __noinline__ bool epi_item(const GemmSeg &sg, uint32_t taddr, 
     }
 }
 // Finish row n of a split tile (GemmSeg::fix_out): add the S partial slabs in
-// slab order, apply the fp16 kind fix_epi, store.  The slabs were written by
+// slab order to zero, apply the fp16 kind fix_epi, store (the same arithmetic
+// as the LoRA finalize kernel, so either path gives the same bits).  The slabs were written by
 // other SMs: read through L2, the loads of up to FIX_BATCH slabs in flight at
 // once (an L2 round trip under the weight stream costs about a microsecond).
 // Columns as in epi_run.
@@ -184,7 +185,7 @@ __device__ __forceinline__ void fix_item(const GemmSeg &sg, int n, int npad, int
                 for (int j = 0; j < FIX_BATCH; ++j)
 #pragma unroll
                     for (int q = 0; q < HW; ++q)
-                        if (j0 + j < sg.S) v[q] = (j0 + j == 0) ? t[j][q] : v[q] + t[j][q];
+                        if (j0 + j < sg.S) v[q] = ((j0 + j == 0) ? 0.0f : v[q]) + t[j][q];
             }
 #pragma unroll
             for (int q = 0; q < HW; ++q) {

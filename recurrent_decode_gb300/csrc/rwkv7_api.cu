@@ -392,15 +392,24 @@ bool ffn_fused(const rwkv7_ctx *c, int mode) {
     return c->wbits == 16 && (mode == 0 || mode == 1) && env_int("RWKV7_FUSE_FFN", 1) != 0;  // tuning knob
 }
 
+int lora_split(const rwkv7_ctx *c, int s1);
+void step_splits(const rwkv7_ctx *c, int *s1, int *s3, int *s5);
+
 // The r, k, v projections, the LoRA down projections and the LoRA up
 // projections with their gates run as one two-phase launch: the LoRA-down
-// items (unsplit, their epilogues write the activated fp16 hidden) are phase 0
-// and counted; the r, k, v items run beside them; the LoRA-up items are phase
-// 1 and read the hidden once every LoRA-down item is stored.  The LoRA chain
-// then overlaps the r, k, v weight stream instead of following it as two more
-// launches.  fp16 tensor-core modes only; otherwise three launches.
-bool att_fused(const rwkv7_ctx *c, int mode) {
-    return c->wbits == 16 && (mode == 0 || mode == 1) && env_int("RWKV7_FUSE_ATT", 1) != 0;  // tuning knob
+// items are phase 0 and counted per finished row tile; the r, k, v items run
+// beside them; the LoRA-up items are phase 1 and read the hidden once every
+// LoRA-down tile is finished.  The LoRA chain then overlaps the r, k, v weight
+// stream instead of following it as two more launches.  fp16 tensor-core
+// modes only; with split LoRA-down tiles only while the batch leaves half the
+// SMs free of the preceding LayerNorm rows (wider batches measured faster as
+// three launches).  Either way the arithmetic is the same, so a slot's result
+// does not depend on which path its step took.
+bool att_fused(const rwkv7_ctx *c, int mode, int B) {
+    if (c->wbits != 16 || (mode != 0 && mode != 1) || env_int("RWKV7_FUSE_ATT", 1) == 0) return false;  // knob
+    int s1, s3, s5;
+    step_splits(c, &s1, &s3, &s5);
+    return lora_split(c, s1) == 1 || 2 * B <= c->nsm;
 }
 
 // nseg0 > 0: a two-phase launch whose first nseg0 segments are phase 0 and
@@ -562,7 +571,7 @@ int run_gemm(rwkv7_ctx *c, int layer, const Seg *segs, int n, int B, uint32_t *n
                 while (gdep < p.g0 && (long long)gdep * p.n0 / p.g0 < p.ndep) ++gdep;
                 const int early = c->nsm - B;
                 const int n1 = p.nitems - p.n0;
-                int pm = !split_dep ? 0 : (early >= gdep + 1 && early >= n1 / 2) ? 3 : 1;
+                int pm = !split_dep ? 0 : (early >= gdep + 1 && early >= n1 / 2) ? 3 : 0;
                 pm = env_int("RWKV7_PHASE1_CTAS", pm);  // tuning knob
                 if (pm == 3) {
                     p.p1a = std::min(early, grid);
@@ -634,7 +643,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
     ep.emb = c->w[W_EMB];
     ep.ln_w = c->w[W_LN0W];
     ep.ln_b = c->w[W_LN0B];
-    const bool fuse_ffn = ffn_fused(c, mode), fuse_att = att_fused(c, mode);
+    const bool fuse_ffn = ffn_fused(c, mode), fuse_att = att_fused(c, mode, B);
     if (fuse_ffn || fuse_att) {  // the per-layer counters of the two-phase launches start at zero every step
         e = cudaMemsetAsync(c->ffn_dep, 0, (2 + FIX_TILES_PER_LAYER) * (size_t)c->L * 4, st);
         if (e != cudaSuccess) return fail(c, RWKV7_ECUDA, "counter reset: %s", cudaGetErrorString(e));
@@ -707,10 +716,11 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
                 return rc;
             pe();
         } else {
-        // G1: r, k, v and the LoRA down projections, as s1 partial slabs.  Without
-        // a k-split the LoRA-down epilogues apply the activation and write the
-        // fp16 hidden themselves (the LoRA finalize kernel would only convert).
-        const bool fin_fused = s1 == 1;
+        // G1: r, k, v as s1 partial slabs and the LoRA down projections as sd
+        // (the fused launch's split).  Without a LoRA-down split the epilogues
+        // apply the activation and write the fp16 hidden themselves (the LoRA
+        // finalize kernel would only convert).
+        const bool fin_fused = sd == 1;
         Seg g1[7];
         int n1 = 0;
         g1[n1++] = {L_WR, A_XR, c->xmix[0], d, EPI_F32, c->pr, d, nullptr, s1};
@@ -722,10 +732,10 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
             if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F16, c->hv, c->rv, nullptr, 1};
             g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F16_SIGMOID, c->hg, c->rg, nullptr, 1};
         } else {
-            g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F32, c->phw, c->rw, nullptr, s1};
-            g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F32, c->pha, c->ra, nullptr, s1};
-            if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F32, c->phv, c->rv, nullptr, s1};
-            g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, s1};
+            g1[n1++] = {L_W1, A_XW, c->xmix[1], d, EPI_F32, c->phw, c->rw, nullptr, sd};
+            g1[n1++] = {L_A1, A_XA, c->xmix[4], d, EPI_F32, c->pha, c->ra, nullptr, sd};
+            if (l > 0) g1[n1++] = {L_V1, A_XV, c->xmix[3], d, EPI_F32, c->phv, c->rv, nullptr, sd};
+            g1[n1++] = {L_G1, A_XG, c->xmix[5], d, EPI_F32, c->phg, c->rg, nullptr, sd};
         }
         pb(P_GEMM_PROJ);
         if ((rc = run_gemm(c, l, g1, n1, B, nullptr, nullptr, lc, mode, tlp(P_GEMM_PROJ)))) return rc;
@@ -735,7 +745,7 @@ int enqueue_step(rwkv7_ctx *c, cudaStream_t st, int B, bool head, bool sample, i
         LoraFinParams lf;
         memset(&lf, 0, sizeof lf);
         lf.B = B;
-        lf.S = s1;
+        lf.S = sd;
         lf.r[0] = c->rw; lf.r[1] = c->ra; lf.r[2] = l > 0 ? c->rv : 0; lf.r[3] = c->rg;
         lf.part[0] = c->phw; lf.part[1] = c->pha; lf.part[2] = c->phv; lf.part[3] = c->phg;
         lf.out[0] = c->hw; lf.out[1] = c->ha; lf.out[2] = c->hv; lf.out[3] = c->hg;
@@ -1603,13 +1613,18 @@ int rwkv7_set_mode(rwkv7_ctx *c, int32_t mode) {
 
 int32_t rwkv7_step_kernel_count(const rwkv7_ctx *c, int32_t B, int32_t with_sampling) {
     if (!c || B < 1) return 0;
-    const int sub = (B + MAX_B - 1) / MAX_B;
     int s1, s3, s5;
     step_splits(c, &s1, &s3, &s5);
-    // the LoRA finalize kernel runs only for a split r, k, v GEMM; the fused
+    // the LoRA finalize kernel runs only for split LoRA-down tiles; the fused
     // channel mix is one launch; the fused r, k, v + LoRA launch replaces three
-    const int per_layer = (att_fused(c, c->mode) ? 6 : (s1 == 1 ? 7 : 8)) + (ffn_fused(c, c->mode) ? 0 : 1);
-    return sub * (1 + per_layer * c->L + 2 + (with_sampling ? 1 : 0));
+    int total = 0;
+    for (int b0 = 0; b0 < B; b0 += MAX_B) {
+        const int nb = std::min(MAX_B, B - b0);
+        const int per_layer = (att_fused(c, c->mode, nb) ? 6 : (lora_split(c, s1) == 1 ? 7 : 8)) +
+                              (ffn_fused(c, c->mode) ? 0 : 1);
+        total += 1 + per_layer * c->L + 2 + (with_sampling ? 1 : 0);
+    }
+    return total;
 }
 
 int rwkv7_ffn_union_stats(rwkv7_ctx *c, uint64_t *nonzero_blocks, uint64_t *blocks) {
