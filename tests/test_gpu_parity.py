@@ -150,6 +150,39 @@ def test_2p9b_layer_sizes_graph_vs_cuda_core():
             assert_logits_close(outs[1][t][i], sts[k].step(int(toks[i])), f"oracle step {t} row {i}")
 
 
+def test_fused_and_three_launch_lora_paths_bit_identical_2p9b():
+    """At the 2.9B layer sizes the LoRA-down tiles are k-split.  A narrow batch
+    runs r, k, v and both LoRA stages as one two-phase launch (each tile's
+    last split adds the slabs); a batch wider than half the SMs runs them as
+    three launches (the finalize kernel adds them).  Both add the same slabs
+    in the same order with the same activations, so a slot fed the same
+    tokens gives bit-identical logits either way."""
+    torch = _torch()
+    dev = torch.device("cuda")
+    W = synth.make_weights("2.9b", n_layer=2)
+    dims = synth.Dims("2.9b", 2)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    wide = min(256, nsm // 2 + 24)
+    ctx, _, _ = gpu_ctx("2.9b", wide + 1, W, 0, n_layer=2)
+    if ctx.step_kernel_count(1, False) == ctx.step_kernel_count(wide, False):
+        ctx.close()
+        pytest.skip("both batch widths take the same path on this device")
+    toks = synth.prompt_tokens(dims.vocab, wide + 1, 3, seed=77)
+    one = torch.empty(1, dims.vocab, device=dev)
+    many = torch.empty(wide, dims.vocab, device=dev)
+    batch_slots = torch.arange(1, wide + 1, dtype=torch.int32, device=dev)
+    pos = wide // 2
+    for t in range(3):
+        ctx.decode_step(torch.zeros(1, dtype=torch.int32, device=dev),
+                        torch.tensor([int(toks[0, t])], dtype=torch.int32, device=dev), one)
+        bt = toks[1:wide + 1, t].copy()
+        bt[pos] = toks[0, t]
+        ctx.decode_step(batch_slots, torch.from_numpy(bt).to(dev), many)
+        ctx.synchronize()
+        assert torch.equal(one[0], many[pos]), f"step {t}"
+    ctx.close()
+
+
 def test_batch_beyond_one_fused_step(tiny):
     """B = 300 slots (more than one fused step of 256): the step runs as two
     sub-steps; rows from both match the oracle, and the host-buffer entry point
