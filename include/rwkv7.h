@@ -324,7 +324,10 @@ RWKV7_API int rwkv7_step_timeline(rwkv7_ctx *ctx, const int32_t *d_slots, const 
                                   int32_t max_launches, int32_t *n_launches);
 
 /* Number of kernels one decode step of B slots launches (with / without
- * sampling), for launch accounting. */
+ * sampling), for launch accounting.  It depends on B: batches wider than
+ * 256 slots run as several fused steps, and where the LoRA-down tiles are k-split
+ * a batch wider than half the SMs runs r, k, v and the two LoRA stages as
+ * three launches instead of one (with the same results). */
 RWKV7_API int32_t rwkv7_step_kernel_count(const rwkv7_ctx *ctx, int32_t B, int32_t with_sampling);
 
 #ifdef __cplusplus
