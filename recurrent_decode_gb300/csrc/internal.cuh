@@ -17,7 +17,7 @@ enum : uint32_t {
     ERR_TOKEN = 2u,    // token id out of range
     ERR_DUP = 4u,      // a slot appears twice in one step
     ERR_TIMEOUT = 8u,  // a bounded wait gave up
-    ERR_CONFIG = 16u,  // a kernel met a launch configuration it cannot run
+    ERR_CONFIG = 16u,  // the sampler found no token to draw (no finite weight)
 };
 
 constexpr int HS = 64;             // head size
