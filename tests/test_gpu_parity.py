@@ -118,8 +118,9 @@ def test_wide_batch_graph_vs_cuda_core(tiny):
 def test_2p9b_layer_sizes_graph_vs_cuda_core():
     """The 2.9B layer sizes (d=2560, F=10240, V=65536, LoRA 96/96/64/320) cut to
     2 layers, B=64 of 72 permuted slots, 3 steps: k-split projections whose
-    slabs the consumers add, the LoRA-up kernel building its activations from
-    the LoRA-down slabs, the 512-tile head.  Every row of the graph-replayed
+    slabs the consumers add, the fused r, k, v + LoRA launch (LoRA-down tiles
+    split in four and finished by their last split, LoRA-up after the
+    in-kernel counter), the 512-tile head.  Every row of the graph-replayed
     tensor-core step (mode 0) matches the CUDA-core cross-check (mode 2) within
     the tolerance and four rows match the oracle."""
     torch = _torch()
