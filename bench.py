@@ -12,6 +12,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -31,11 +32,11 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 # dram bytes per launch from ncu captures, valid only while the kernel source is
-# unchanged: kernel -> (source files, sha256 prefix of their concatenation at
-# capture, workload, bytes)
+# unchanged: kernel -> (source files, sha256 prefix of their code without
+# comments and blank lines at capture, workload, bytes)
 NCU_TRAFFIC = {
     ("gemm_tc_kernel", "2.9b"): (("recurrent_decode_gb300/csrc/gemm.cu", "recurrent_decode_gb300/csrc/gemm_common.cuh"),
-                                  "954915d205220eda",
+                                  "61ffbca0c231fdc5",
                                   "2.9B shape, B=64: DRAM read+write of the 7 GEMM launches of one step of "
                                   "a 2-layer cut (ncu), scaled to 32 layers + head, "
                                   "per launch", 59051560),
@@ -51,11 +52,19 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines, so that a hash of it
+    changes with the code and not with its documentation."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def _sha(paths):
     h = hashlib.sha256()
     for path in paths:
-        with open(path, "rb") as fh:
-            h.update(fh.read())
+        with open(path, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -17,7 +17,12 @@
 //    (gemm_common.cuh).  Work items are
 //    (row tile, k-range) pairs split evenly over the grid; a split k-range
 //    stores fp32 partial sums that the consuming kernel adds in a fixed order,
-//    so no CTA waits for another and results do not depend on timing.
+//    so results do not depend on timing.  A two-phase launch chains two
+//    dependent projections in one grid (every CTA resident): its phase-1
+//    activations are read once an in-kernel counter shows the phase-0 items
+//    that produce them stored (bounded waits), and a split phase-0 tile may
+//    be finished in the launch by its last split (an atomic ticket picks it;
+//    it adds the slabs in slab order).
 //  * SIMT kernel: a plain warp-per-row dot product with the same epilogues and
 //    partial layout, kept as an independent cross-check of the tensor-core kernel.
 // The int8-weight variant of the tensor-core kernel is in gemm8.cu.
