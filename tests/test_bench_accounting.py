@@ -40,3 +40,16 @@ def test_headline_bytes_per_step():
     # weights + states per step of the 2.9B (B = 64) and 7.2B (B = 256) decode workloads
     assert round(bench.step_bytes(synth.Dims("2.9b"), 64) / 1e9, 3) == 8.326
     assert round(bench.step_bytes(synth.Dims("7.2b"), 256) / 1e9, 3) == 31.575
+
+
+def test_traffic_hash_follows_code_not_comments(tmp_path):
+    """The ncu traffic record stays valid across comment edits of the kernel
+    source and is dropped on any code edit."""
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int *p) {\n    p[0] = 1;  // store\n}\n")
+    h0 = bench._sha([str(src)])
+    src.write_text("// header, reworded\n/* a block\n   comment */\n__global__ void k(int *p) {\n\n    p[0] = 1;\n}\n")
+    assert bench._sha([str(src)]) == h0
+    src.write_text("// header\n__global__ void k(int *p) {\n    p[0] = 2;  // store\n}\n")
+    assert bench._sha([str(src)]) != h0
+
